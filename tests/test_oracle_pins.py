@@ -1,0 +1,271 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each test names what fixes the expected value: a library conversion, an
+exhaustive sweep, exact rational arithmetic, a closed form, a hand-worked
+example, or a planted mistake that must be caught.
+"""
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ALL16 = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+
+
+# ---------------------------------------------------------------- formats
+def test_fp16_decode_matches_numpy_all_patterns():
+    ours = oracle.fp16_to_f64(ALL16)
+    ref = ALL16.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    # signed zeros are distinct patterns with the right sign
+    assert np.signbit(oracle.fp16_to_f64(np.uint16(0x8000)))
+    assert not np.signbit(oracle.fp16_to_f64(np.uint16(0x0000)))
+
+
+def test_bf16_decode_matches_torch_all_patterns():
+    ours = oracle.bf16_to_f64(ALL16)
+    ref = torch.from_numpy(ALL16.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def test_fp16_rounding_is_nearest_even_at_every_midpoint():
+    # every pair of adjacent positive finite FP16 values, including subnormals
+    lo = np.arange(0, 0x7BFF, dtype=np.uint16)
+    a = oracle.fp16_to_f64(lo)
+    b = oracle.fp16_to_f64(lo + 1)
+    mid = (a + b) / 2                       # exact in fp64
+    r = oracle.f64_to_fp16_bits(mid)
+    even = np.where(lo % 2 == 0, lo, lo + 1)
+    assert np.array_equal(r, even)
+    # just below / above the midpoint goes to the nearer value
+    below = np.nextafter(mid, -np.inf)
+    above = np.nextafter(mid, np.inf)
+    assert np.array_equal(oracle.f64_to_fp16_bits(below), lo)
+    assert np.array_equal(oracle.f64_to_fp16_bits(above), lo + 1)
+    # overflow threshold: 65504 + half an ulp (16) rounds to inf (ties to even)
+    assert oracle.f64_to_fp16_bits(65519.99) == 0x7BFF
+    assert oracle.f64_to_fp16_bits(65520.0) == 0x7C00
+    # negative values mirror positive ones
+    assert np.array_equal(oracle.f64_to_fp16_bits(-mid), even | 0x8000)
+
+
+# ---------------------------------------------------------------- encoder
+def _nearest_fp16_exact(q: Fraction) -> int:
+    """Nearest FP16 pattern to a positive rational, ties to even, by search."""
+    approx = int(np.float64(float(q)).astype(np.float16).view(np.uint16))
+    best = None
+    for p in range(max(0, approx - 2), min(0x7C00, approx + 3)):
+        v = Fraction(float(oracle.fp16_to_f64(np.uint16(p))))
+        d = abs(v - q)
+        key = (d, p % 2)
+        if best is None or key < best[0]:
+            best = (key, p)
+    return best[1]
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6])
+def test_rtn_scale_is_exact_nearest_fp16(bits):
+    rng = synth.generator(0, 100, bits)
+    w = synth.gauss_weights(rng, 64, 64 * 8)
+    # add groups with tiny and subnormal-scale magnitudes
+    w[0, :64] *= np.float32(1e-5)
+    w[1, :64] *= np.float32(1e-7)
+    s = oracle.rtn_scales(w, oracle.QMAX[bits])
+    a = np.abs(w.reshape(64, 8, 64)).max(axis=2)
+    for i in range(64):
+        for g in range(8):
+            q = Fraction(float(a[i, g])) / oracle.QMAX[bits]
+            assert s[i, g] == _nearest_fp16_exact(q), (i, g)
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6])
+def test_rtn_code_is_brute_force_nearest(bits):
+    rng = synth.generator(0, 101, bits)
+    n, k = 8, 256
+    w = synth.gauss_weights(rng, n, k)
+    codes, sb = oracle.rtn_encode(w, bits)
+    lo, hi = oracle.code_range(bits)
+    s = oracle.fp16_to_f64(sb)
+    for i in range(n):
+        for j in range(k):
+            sv = Fraction(float(s[i, j // 64]))
+            wv = Fraction(float(w[i, j]))
+            best = min(range(lo, hi + 1), key=lambda c: (abs(wv - sv * c), c % 2))
+            assert codes[i, j] == best, (i, j)
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6])
+def test_rtn_invariants(bits):
+    rng = synth.generator(0, 102, bits)
+    w = synth.gauss_weights(rng, 64, 1024)
+    codes, sb = oracle.rtn_encode(w, bits)
+    qmax = oracle.QMAX[bits]
+    assert codes.min() >= -qmax and codes.max() <= qmax   # positive scale: no -qmax-1
+    s = np.repeat(oracle.fp16_to_f64(sb), 64, axis=1)
+    err = np.abs(w.astype(np.float64) - s * codes)
+    clamped = np.abs(codes) == qmax
+    assert np.all(err[~clamped] <= s[~clamped] / 2)
+    # the group maximum lands on +-qmax
+    amax_idx = np.abs(w.reshape(64, 16, 64)).argmax(axis=2)
+    c_at = np.take_along_axis(codes.reshape(64, 16, 64), amax_idx[..., None], axis=2)
+    assert np.all(np.abs(c_at) == qmax)
+
+
+def test_rtn_zero_group_and_overflow():
+    w = np.zeros((1, 128), dtype=np.float32)
+    w[0, 64:] = 1.0
+    codes, sb = oracle.rtn_encode(w, 4)
+    assert sb[0, 0] == 0 and np.all(codes[0, :64] == 0)
+    assert np.all(codes[0, 64:] == 7)
+    big = np.full((1, 64), 7.0 * 65520.0, dtype=np.float32)
+    with pytest.raises(ValueError):
+        oracle.rtn_encode(big, 4)
+
+
+def test_worked_example_golden():
+    with open(os.path.join(HERE, "golden", "rtn_worked_example.json")) as f:
+        g = json.load(f)
+    w = np.zeros((1, 64), dtype=np.float32)
+    for k, v in g["weights_fp32_nonzero"].items():
+        w[0, int(k)] = v
+    for case in g["cases"]:
+        codes, sb = oracle.rtn_encode(w, case["bits"])
+        assert int(sb[0, 0]) == int(case["scale_bits"], 16)
+        assert oracle.fp16_to_f64(sb[0, 0]) == case["scale"]
+        assert list(codes[0, :3]) == case["codes_first3"]
+        assert np.all(codes[0, 3:] == 0)
+    p = g["product"]
+    codes, sb = oracle.rtn_encode(w, p["bits"])
+    x = np.zeros((1, 64), dtype=np.float32)
+    for k, v in p["x_nonzero"].items():
+        x[0, int(k)] = v
+    xb = (x.view(np.uint32) >> 16).astype(np.uint16)   # exact: these are bf16 values
+    y, e = oracle.gemv(codes, sb, xb)
+    assert y[0, 0] == p["y"] and e[0, 0] == p["E"]
+
+
+# ---------------------------------------------------------------- dequant
+def test_dequant_exact_all_fp16_times_all_codes():
+    finite = ALL16[(ALL16 & 0x7C00) != 0x7C00]
+    s = oracle.fp16_to_f64(finite)[:, None]
+    c = np.arange(-32, 32, dtype=np.float64)[None, :]
+    p = s * c
+    # exact in fp32: casting to fp32 and back loses nothing
+    assert np.array_equal(p.astype(np.float32).astype(np.float64), p)
+    # and the oracle's dequant gives exactly these products
+    codes = np.tile(np.arange(-32, 32, dtype=np.int8), (finite.size, 1))
+    w = oracle.dequant(codes, finite[:, None])
+    assert np.array_equal(w, p)
+    # signed zero: -0 scale times positive code is -0
+    assert np.signbit(oracle.dequant(np.full((1, 64), 3, np.int8), np.array([[0x8000]], np.uint16)))[0, 0]
+
+
+def test_dequant_matches_rationals_sample():
+    rng = synth.generator(0, 103)
+    sb = rng.integers(0, 0x7C00, size=(4, 4), dtype=np.uint16) | (rng.integers(0, 2, (4, 4), dtype=np.uint16) << 15)
+    codes = synth.uniform_codes(rng, 4, 256, 6)
+    w = oracle.dequant(codes, sb)
+    for i in range(4):
+        for j in range(0, 256, 7):
+            sv = Fraction(float(oracle.fp16_to_f64(sb[i, j // 64])))
+            assert Fraction(float(w[i, j])) == sv * int(codes[i, j])
+
+
+# ---------------------------------------------------------------- product
+@pytest.mark.parametrize("bits,k,n,t", [(4, 64, 3, 1), (5, 128, 4, 2), (6, 256, 8, 4), (6, 192, 5, 3)])
+def test_gemv_against_exact_rationals(bits, k, n, t):
+    rng = synth.generator(0, 104, bits, k)
+    codes = synth.uniform_codes(rng, n, k, bits)
+    sb = oracle.rtn_scales(synth.gauss_weights(rng, n, k), oracle.QMAX[bits])
+    sb = sb ^ (synth.sign_flips(rng, n, k // 64).astype(np.uint16) << 15)
+    xb = synth.gauss_x_bf16(rng, t, k, outliers=synth.outlier_channels(rng, k, 0.05))
+    y, e = oracle.gemv(codes, sb, xb)
+    s = oracle.fp16_to_f64(sb)
+    xv = oracle.bf16_to_f64(xb)
+    for ti in range(t):
+        for ni in range(n):
+            exact = sum(Fraction(float(s[ni, kk // 64])) * int(codes[ni, kk]) * Fraction(float(xv[ti, kk]))
+                        for kk in range(k))
+            eabs = sum(abs(Fraction(float(s[ni, kk // 64])) * int(codes[ni, kk]) * Fraction(float(xv[ti, kk])))
+                       for kk in range(k))
+            # fp64 summation error bound: K * 2^-53 * sum|terms|
+            assert abs(Fraction(float(y[ti, ni])) - exact) <= Fraction(k, 2 ** 53) * eabs
+            assert abs(Fraction(float(e[ti, ni])) - eabs) <= Fraction(k, 2 ** 53) * eabs
+
+
+def test_special_cases():
+    rng = synth.generator(0, 105)
+    n, k = 6, 256
+    codes = synth.uniform_codes(rng, n, k, 5)
+    sb = oracle.rtn_scales(synth.gauss_weights(rng, n, k), 15)
+    w = oracle.dequant(codes, sb)
+    # one-hot x reproduces a column of w exactly
+    for kk in (0, 63, 64, 200):
+        x = np.zeros((1, k), np.uint16)
+        x[0, kk] = 0x3F80           # bf16 1.0
+        y, _ = oracle.gemv(codes, sb, x)
+        assert np.array_equal(y[0], w[:, kk])
+    # zero codes give zero
+    y, e = oracle.gemv(np.zeros_like(codes), sb, synth.gauss_x_bf16(rng, 2, k))
+    assert np.all(y == 0) and np.all(e == 0)
+    # x = 1 on one group gives s * sum(c) exactly
+    x = np.zeros((1, k), np.uint16)
+    x[0, 64:128] = 0x3F80
+    y, _ = oracle.gemv(codes, sb, x)
+    ref = oracle.fp16_to_f64(sb[:, 1]) * codes[:, 64:128].astype(np.int64).sum(axis=1)
+    assert np.array_equal(y[0], ref)
+    # negating every scale negates the output exactly
+    xb = synth.gauss_x_bf16(rng, 3, k)
+    y1, e1 = oracle.gemv(codes, sb, xb)
+    y2, e2 = oracle.gemv(codes, sb ^ np.uint16(0x8000), xb)
+    assert np.array_equal(y1, -y2) and np.array_equal(e1, e2)
+
+
+# ---------------------------------------------------------------- tolerance sensitivity
+def _planted(codes, sb, xb, kind):
+    """The oracle's product with one deliberate mistake."""
+    c = codes.astype(np.float64)
+    n, k = codes.shape
+    s = oracle.fp16_to_f64(sb)
+    if kind == "group_off_by_one":
+        idx = np.minimum((np.arange(k) + 1) // 64, k // 64 - 1)
+        w = s[:, idx] * c
+    elif kind == "scale_sign_dropped":
+        w = np.repeat(np.abs(s), 64, axis=1) * c
+    elif kind == "code_bias":
+        w = np.repeat(s, 64, axis=1) * (c + 1)
+    elif kind == "k_pairs_swapped":
+        perm = np.arange(k).reshape(-1, 2)[:, ::-1].reshape(-1)
+        w = np.repeat(s, 64, axis=1) * c[:, perm]
+    elif kind == "tokens_swapped":
+        w = np.repeat(s, 64, axis=1) * c
+        return oracle.bf16_to_f64(xb[::-1]) @ w.T
+    else:
+        raise ValueError(kind)
+    return oracle.bf16_to_f64(xb) @ w.T
+
+
+@pytest.mark.parametrize("kind", ["group_off_by_one", "scale_sign_dropped", "code_bias",
+                                  "k_pairs_swapped", "tokens_swapped"])
+def test_tolerance_catches_planted_mistakes(kind):
+    rng = synth.generator(0, 106)
+    n, k, t = 32, 1024, 2
+    codes = synth.uniform_codes(rng, n, k, 5)
+    sb = oracle.rtn_scales(synth.gauss_weights(rng, n, k), 15)
+    sb = sb ^ (synth.sign_flips(rng, n, k // 64).astype(np.uint16) << 15)
+    xb = synth.gauss_x_bf16(rng, t, k, outliers=synth.outlier_channels(rng, k))
+    y, e = oracle.gemv(codes, sb, xb)
+    bad = _planted(codes, sb, xb, kind)
+    assert oracle.tolerance_ok(y.astype(np.float32), y, e)
+    assert not oracle.tolerance_ok(bad, y, e)
