@@ -1,0 +1,176 @@
+/*
+ * nq.h -- C ABI of the groupwise-quantized small-T GEMV library (libnq.so).
+ *
+ * Operation (page "Qwen3.8-27B for NInfer on the RTX 3090", section "What is
+ * different from the upstream artifact"): a weight matrix W[N, K] is stored as
+ * signed integer codes c in groups of 64 consecutive weights along K, with one
+ * FP16 scale s per group, and w = s * c.  Code widths: 4 bits [-8, 7],
+ * 5 bits [-16, 15], 6 bits [-32, 31].  Scales may be negative.  The library
+ * computes
+ *
+ *        y[t, n] = sum_k x[t, k] * s[n, k / 64] * c[n, k]      t < T <= 16
+ *
+ * with x in bf16 and y in fp32: the decode and speculative-verify matrix
+ * products of the engine described on that page and on "giveen/ninfer-ext"
+ * (sections "Where ninfer-ext leads" and "Engineering": small-batch K-split
+ * routes for the verify rounds of speculative decoding).
+ *
+ * Conventions shared by every entry point
+ *   - Return value: NQ_OK (0) or a negative nq_status.  Validation happens on
+ *     the host before any launch; a failed validation launches nothing and
+ *     writes nothing.
+ *   - The caller owns every buffer; no call allocates memory.
+ *   - "device" pointers are CUDA device pointers (current device); "host"
+ *     pointers are ordinary CPU memory.  Device pointers must be 16-byte
+ *     aligned (NQ_EALIGN otherwise).
+ *   - Device entry points are asynchronous on `stream` (0 = legacy default
+ *     stream).  A launch failure is reported as NQ_ECUDA (the CUDA error is
+ *     consumed).  Errors found by a running kernel (a bounded wait that gave
+ *     up, a scale that overflowed) are recorded in a per-device status word
+ *     that nq_last_device_error() reads and clears.
+ *   - Thread-safe: no state besides the per-device status word and cached
+ *     per-device launch settings.
+ *
+ * PACKED LAYOUT (version 1)
+ * -------------------------
+ *   Rows are taken in tiles of 16 (Nt = ceil(N/16) tiles; rows >= N of the
+ *   last tile are padding with code 0 and scale +0), groups of 64 along K
+ *   (G = K/64).  One "block" holds the codes of one row tile and one group,
+ *   1024 codes, split among 32 lanes: lane L (q = L/4, r = L%4) owns 32 codes,
+ *   16 pairs p = 4*j + i (j = 0..3 sixteen-wide K slices, i = 0..3):
+ *       i = 0: row q,     k = 16j + 2r + {0, 1}
+ *       i = 1: row q + 8, k = 16j + 2r + {0, 1}
+ *       i = 2: row q,     k = 16j + 2r + 8 + {0, 1}
+ *       i = 3: row q + 8, k = 16j + 2r + 8 + {0, 1}
+ *   (k relative to the group).  Every code is stored biased, u = c + 2^(b-1),
+ *   as an unsigned b-bit field.  The first code of a pair sits in the low
+ *   16-bit half of a 32-bit word, the second at the same offset + 16.
+ *   A lane's words (W = b 32-bit words) are:
+ *     4 bits: word j holds pairs 4j..4j+3; pair i at bit offset 4i.
+ *     5 bits: 5 words; each half has three 5-bit fields at offsets 0, 5, 10
+ *             holding pairs p = 3w + f (w word, f field) for p < 15; pair 15
+ *             is spread over bit 15 of each half: bit m of its code is bit 15
+ *             of word m (low code) / bit 31 of word m (high code).
+ *     6 bits: 6 words; each half has two 6-bit fields at offsets 0 and 6
+ *             holding pairs p = 2w + f for p < 12; pairs 12..15 (d = p - 12)
+ *             take bits 0..3 of their code from bits 12..15 of word d and
+ *             bits 4..5 from bits 12 + 2(d%2) .. 13 + 2(d%2) of word
+ *             4 + d/2 (same offsets + 16 for the high code).
+ *   Inside a block, words 0..3 of all lanes come first (lane L at byte
+ *   16 L), then the remaining words (lane L at 512 + 4(W-4) L).  Block size:
+ *   512 / 640 / 768 bytes for 4 / 5 / 6 bits.  Blocks are ordered
+ *   [row tile][group]; codes bytes = Nt * G * block size.
+ *   Scales: [row tile][group][8][2] FP16, entry (m, h) = row m + 8h of the
+ *   tile; 32 bytes per block; scales bytes = Nt * G * 32.
+ */
+#ifndef NQ_H
+#define NQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so the header needs no CUDA headers. */
+typedef struct CUstream_st* nq_stream_t;
+
+typedef enum {
+  NQ_OK = 0,
+  NQ_EINVAL = -1,        /* bad size, width, T, route, or null pointer */
+  NQ_EALIGN = -2,        /* device pointer not 16-byte aligned */
+  NQ_ERANGE = -3,        /* code outside its range, non-finite or overflowing scale */
+  NQ_ECUDA = -4,         /* CUDA launch or runtime error */
+  NQ_ETIMEOUT = -5,      /* a kernel's bounded wait gave up (reported by nq_last_device_error) */
+  NQ_EUNSUPPORTED = -6   /* shape needs more shared memory than one cluster provides */
+} nq_status;
+
+/* Kernel route of nq_gemv_ex. */
+typedef enum {
+  NQ_ROUTE_AUTO = 0,     /* library choice (see NQ_ROUTE environment variable) */
+  NQ_ROUTE_MMA = 1,      /* warp-level bf16 tensor-core MMA, fp32 accumulate, T <= 16 */
+  NQ_ROUTE_FFMA = 2      /* CUDA-core fp32 FMA, T <= 4 */
+} nq_route;
+
+/* Byte sizes of the packed codes and packed scales of a W[N, K] tensor.
+ * K % 64 == 0, K > 0, N > 0, bits in {4, 5, 6}; outputs are host pointers. */
+int nq_packed_bytes(int64_t K, int64_t N, int bits, size_t* codes_bytes, size_t* scales_bytes);
+
+/* Host packer.  codes: host int8 [N, K] row-major, values in the signed range
+ * of `bits`; scales: host FP16 bit patterns [N, K/64] row-major, finite.
+ * Writes packed_out (codes_bytes) and scales_out (scales_bytes / 2 entries),
+ * both host, caller-allocated.  NQ_ERANGE on an out-of-range code or a
+ * non-finite scale (nothing is written in that case). */
+int nq_pack(const int8_t* codes, const uint16_t* scales, int64_t K, int64_t N, int bits,
+            void* packed_out, uint16_t* scales_out);
+
+/* Host inverse of nq_pack (test and inspection aid).  All pointers host. */
+int nq_unpack(const void* packed, const uint16_t* scales_packed, int64_t K, int64_t N, int bits,
+              int8_t* codes_out, uint16_t* scales_out);
+
+/* Device packer: same layout as nq_pack, for tensors already in device memory.
+ * codes, scales, packed_out, scales_out are device pointers.  Range errors
+ * are not checked here (use nq_pack or check beforehand). */
+int nq_pack_device(const int8_t* codes, const uint16_t* scales, int64_t K, int64_t N, int bits,
+                   void* packed_out, uint16_t* scales_out, nq_stream_t stream);
+
+/* Device round-to-nearest encoder (the "upstream" encoder of the page named
+ * above): per 64-group, scale = FP16 round-to-nearest-even of max|w| / qmax
+ * (qmax = 7 / 15 / 31) and code = round-half-even(w / scale) clamped to the
+ * code range; an all-zero group gives scale +0 and codes 0.
+ * w: device fp32 [N, K]; codes_out: device int8 [N, K]; scales_out: device
+ * FP16 bits [N, K/64].  A scale that overflows FP16 sets NQ_ERANGE in the
+ * device status word. */
+int nq_quantize_rtn(const float* w, int64_t K, int64_t N, int bits,
+                    int8_t* codes_out, uint16_t* scales_out, nq_stream_t stream);
+
+/* y[T, N] (fp32, device, row-major, overwritten) = x[T, K] (bf16 bit
+ * patterns, device, row-major) times dequant(W)^T, W given by its packed codes
+ * and packed scales (device, layout above).  1 <= T <= 16.
+ * NQ_EUNSUPPORTED if K * T is too large for the shared-memory x tile
+ * (K * T <= 327680 is always supported). */
+int nq_gemv(const void* packed, const uint16_t* scales, const void* x_bf16, float* y,
+            int64_t K, int64_t N, int T, int bits, nq_stream_t stream);
+
+/* nq_gemv with an explicit kernel route and K-split (cluster size).
+ * route: nq_route; ksplit: 0 = automatic, else 1, 2, 4 or 8 CTAs per cluster
+ * splitting K.  NQ_EINVAL if the route does not support T. */
+int nq_gemv_ex(const void* packed, const uint16_t* scales, const void* x_bf16, float* y,
+               int64_t K, int64_t N, int T, int bits, int route, int ksplit, nq_stream_t stream);
+
+/* Dequantised weights w[N, K] fp32 (device, row-major) = scale * code, exact.
+ * Test aid: lets the decode path be checked bit for bit. */
+int nq_dequant(const void* packed, const uint16_t* scales, float* w, int64_t K, int64_t N,
+               int bits, nq_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the current device's status
+ * word: NQ_OK, NQ_ETIMEOUT, NQ_ERANGE, or NQ_ECUDA if the synchronisation
+ * itself failed. */
+int nq_last_device_error(nq_stream_t stream);
+
+/* Launch plan nq_gemv_ex would use (for tests and benchmarks): writes the
+ * route, the K-split, the number of clusters, the pipeline stages and the
+ * dynamic shared memory in bytes to the non-null host pointers.  Needs a
+ * current CUDA device. */
+int nq_gemv_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit,
+                 int* route_out, int* ksplit_out, int* clusters_out, int* stages_out,
+                 int* smem_out);
+
+/* Self-test of the bounded waits: launches one CTA that waits on a barrier
+ * nothing will ever complete, with a limit of `limit_us` microseconds; the
+ * kernel then gives up, records NQ_ETIMEOUT in the status word and returns.
+ * The caller reads the result with nq_last_device_error(stream). */
+int nq_selftest_wait_timeout(int limit_us, nq_stream_t stream);
+
+/* Static description of a status code. */
+const char* nq_status_string(int status);
+
+/* Packed-layout version implemented by this library (1). */
+int nq_layout_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NQ_H */

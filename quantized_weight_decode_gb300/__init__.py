@@ -1,0 +1,242 @@
+"""Python binding of libnq.so, the groupwise-quantized small-T GEMV library.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI of ``include/nq.h``.  PyTorch is used for device
+memory and streams (tensors pass their ``data_ptr()``, streams their
+``cuda_stream`` handle).  The library must have been built (``build()`` below
+or ``python quantized_weight_decode_gb300/buildlib.py``); importing works without
+it, but every call raises if it is missing -- there is no fallback path.
+
+Names follow the C ABI: ``gemv`` is ``nq_gemv``, ``pack`` is ``nq_pack`` ...
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+__all__ = [
+    "NQError", "ROUTE_AUTO", "ROUTE_MMA", "ROUTE_FFMA", "lib", "lib_path", "build",
+    "packed_bytes", "pack", "unpack", "pack_device", "quantize_rtn", "gemv", "dequant",
+    "last_device_error", "plan", "selftest_wait_timeout", "status_string", "layout_version",
+    "QuantizedWeight", "EXPORTED",
+]
+
+ROUTE_AUTO, ROUTE_MMA, ROUTE_FFMA = 0, 1, 2
+OK, EINVAL, EALIGN, ERANGE, ECUDA, ETIMEOUT, EUNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libnq.so")
+_lib = None
+_lock = threading.Lock()
+
+# Every symbol declared in include/nq.h, with its ctypes signature.
+_i64, _i32, _vp, _szp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes.c_size_t)
+_ip = ctypes.POINTER(ctypes.c_int)
+_SIGS = {
+    "nq_packed_bytes": (_i32, [_i64, _i64, _i32, _szp, _szp]),
+    "nq_pack": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _vp]),
+    "nq_unpack": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _vp]),
+    "nq_pack_device": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp]),
+    "nq_quantize_rtn": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _vp]),
+    "nq_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
+    "nq_gemv_ex": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp]),
+    "nq_dequant": (_i32, [_vp, _vp, _vp, _i64, _i64, _i32, _vp]),
+    "nq_last_device_error": (_i32, [_vp]),
+    "nq_gemv_plan": (_i32, [_i64, _i64, _i32, _i32, _i32, _i32, _ip, _ip, _ip, _ip, _ip]),
+    "nq_selftest_wait_timeout": (_i32, [_i32, _vp]),
+    "nq_status_string": (ctypes.c_char_p, [_i32]),
+    "nq_layout_version": (_i32, []),
+}
+EXPORTED = tuple(_SIGS)
+
+
+class NQError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def build(force: bool = False) -> str:
+    """Compile libnq.so for sm_103a in-tree (needs nvcc)."""
+    from . import buildlib as _b
+    return _b.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"{_LIB_PATH} is missing: build it with quantized_weight_decode_gb300.build() "
+                    "(there is no fallback implementation)")
+            h = ctypes.CDLL(_LIB_PATH)
+            for name, (res, args) in _SIGS.items():
+                f = getattr(h, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = h
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().nq_status_string(int(code)).decode()
+
+
+def layout_version() -> int:
+    return int(lib().nq_layout_version())
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != OK:
+        raise NQError(rc, where)
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _dptr(t) -> int:
+    return int(t.data_ptr())
+
+
+# ---------------------------------------------------------------- host side
+def packed_bytes(K: int, N: int, bits: int) -> tuple[int, int]:
+    cb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().nq_packed_bytes(K, N, bits, ctypes.byref(cb), ctypes.byref(sb)), "nq_packed_bytes")
+    return cb.value, sb.value
+
+
+def pack(codes: np.ndarray, scales: np.ndarray, bits: int) -> tuple[np.ndarray, np.ndarray]:
+    """Host packer: int8 codes [N, K] and FP16 scale bits [N, K/64] -> packed
+    codes (uint8) and packed scales (uint16), as numpy arrays."""
+    codes = np.ascontiguousarray(codes, dtype=np.int8)
+    scales = np.ascontiguousarray(scales).view(np.uint16)
+    N, K = codes.shape
+    cb, sb = packed_bytes(K, N, bits)
+    out = np.empty(cb, dtype=np.uint8)
+    sout = np.empty(sb // 2, dtype=np.uint16)
+    _check(lib().nq_pack(codes.ctypes.data, scales.ctypes.data, K, N, bits,
+                         out.ctypes.data, sout.ctypes.data), "nq_pack")
+    return out, sout
+
+
+def unpack(packed: np.ndarray, scales_packed: np.ndarray, K: int, N: int,
+           bits: int) -> tuple[np.ndarray, np.ndarray]:
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    scales_packed = np.ascontiguousarray(scales_packed).view(np.uint16)
+    codes = np.empty((N, K), dtype=np.int8)
+    scales = np.empty((N, K // 64), dtype=np.uint16)
+    _check(lib().nq_unpack(packed.ctypes.data, scales_packed.ctypes.data, K, N, bits,
+                           codes.ctypes.data, scales.ctypes.data), "nq_unpack")
+    return codes, scales
+
+
+# ---------------------------------------------------------------- device side
+def pack_device(codes, scales, bits: int, packed=None, scales_packed=None, stream=None):
+    """Device packer.  codes: int8 cuda [N, K]; scales: 16-bit cuda [N, K/64].
+    Returns (packed uint8 tensor, packed scales int16 tensor)."""
+    import torch
+    N, K = codes.shape
+    cb, sb = packed_bytes(K, N, bits)
+    if packed is None:
+        packed = torch.empty(cb, dtype=torch.uint8, device=codes.device)
+    if scales_packed is None:
+        scales_packed = torch.empty(sb // 2, dtype=torch.int16, device=codes.device)
+    _check(lib().nq_pack_device(_dptr(codes), _dptr(scales), K, N, bits, _dptr(packed),
+                                _dptr(scales_packed), _stream_handle(stream)), "nq_pack_device")
+    return packed, scales_packed
+
+
+def quantize_rtn(w, bits: int, codes=None, scales=None, stream=None):
+    """Device round-to-nearest encoder: fp32 cuda w [N, K] -> (int8 codes [N, K],
+    int16 FP16-scale bits [N, K/64])."""
+    import torch
+    N, K = w.shape
+    if codes is None:
+        codes = torch.empty((N, K), dtype=torch.int8, device=w.device)
+    if scales is None:
+        scales = torch.empty((N, K // 64), dtype=torch.int16, device=w.device)
+    _check(lib().nq_quantize_rtn(_dptr(w), K, N, bits, _dptr(codes), _dptr(scales),
+                                 _stream_handle(stream)), "nq_quantize_rtn")
+    return codes, scales
+
+
+def gemv(packed, scales, x, y, K: int, N: int, T: int, bits: int, route: int = ROUTE_AUTO,
+         ksplit: int = 0, stream=None) -> None:
+    """y[T, N] (fp32 cuda) = x[T, K] (bf16 cuda) @ dequant(W)^T, asynchronous."""
+    if route == ROUTE_AUTO and ksplit == 0:
+        rc = lib().nq_gemv(_dptr(packed), _dptr(scales), _dptr(x), _dptr(y), K, N, T, bits,
+                           _stream_handle(stream))
+    else:
+        rc = lib().nq_gemv_ex(_dptr(packed), _dptr(scales), _dptr(x), _dptr(y), K, N, T, bits,
+                              route, ksplit, _stream_handle(stream))
+    _check(rc, "nq_gemv")
+
+
+def dequant(packed, scales, K: int, N: int, bits: int, out=None, stream=None):
+    import torch
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=packed.device)
+    _check(lib().nq_dequant(_dptr(packed), _dptr(scales), _dptr(out), K, N, bits,
+                            _stream_handle(stream)), "nq_dequant")
+    return out
+
+
+def last_device_error(stream=None) -> int:
+    """Synchronise the stream, return and clear the device status word."""
+    return int(lib().nq_last_device_error(_stream_handle(stream)))
+
+
+def plan(K: int, N: int, T: int, bits: int, route: int = ROUTE_AUTO, ksplit: int = 0) -> dict:
+    vals = [ctypes.c_int() for _ in range(5)]
+    _check(lib().nq_gemv_plan(K, N, T, bits, route, ksplit, *[ctypes.byref(v) for v in vals]),
+           "nq_gemv_plan")
+    keys = ("route", "ksplit", "clusters", "stages", "smem")
+    return {k: v.value for k, v in zip(keys, vals)}
+
+
+def selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    _check(lib().nq_selftest_wait_timeout(limit_us, _stream_handle(stream)),
+           "nq_selftest_wait_timeout")
+
+
+class QuantizedWeight:
+    """A packed weight W[N, K] resident on the device, with its GEMV."""
+
+    def __init__(self, packed, scales, K: int, N: int, bits: int):
+        self.packed, self.scales, self.K, self.N, self.bits = packed, scales, K, N, bits
+
+    @classmethod
+    def from_fp32(cls, w, bits: int, stream=None) -> "QuantizedWeight":
+        codes, scales = quantize_rtn(w, bits, stream=stream)
+        packed, sp = pack_device(codes, scales, bits, stream=stream)
+        N, K = w.shape
+        return cls(packed, sp, K, N, bits)
+
+    @property
+    def nbytes(self) -> int:
+        return self.packed.numel() + 2 * self.scales.numel()
+
+    def gemv(self, x, y=None, route: int = ROUTE_AUTO, ksplit: int = 0, stream=None):
+        import torch
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty((T, self.N), dtype=torch.float32, device=x.device)
+        gemv(self.packed, self.scales, x, y, self.K, self.N, T, self.bits, route, ksplit, stream)
+        return y

@@ -1,0 +1,195 @@
+// Auxiliary device kernels: device packer, round-to-nearest encoder,
+// dequantisation (test aid), the bounded-wait self-test, and the per-device
+// status word that kernels use to report errors.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gemv.cuh"
+#include "layout.h"
+#include "ptx.cuh"
+
+namespace nq {
+
+__device__ int g_status_word;  // per device: first error a kernel recorded
+
+int* device_status_ptr() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
+
+// ------------------------------------------------------------------ packer
+// One thread per (row tile, group, lane): gathers the lane's 32 codes from the
+// row-major code matrix and writes its words; lanes 0..15 also write the
+// scale of row `lane` of the tile.
+template <int BITS>
+__global__ void pack_kernel(const int8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
+                            long long K, long long N, int G, long long nthreads,
+                            uint8_t* __restrict__ packed, uint16_t* __restrict__ scales_out) {
+  const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (tid >= nthreads) return;
+  const int lane = static_cast<int>(tid & 31);
+  const long long blk = tid >> 5;  // rt * G + g
+  const long long rt = blk / G;
+  const int g = static_cast<int>(blk - rt * G);
+  uint32_t u[32];
+#pragma unroll
+  for (int p = 0; p < 16; ++p) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      int row, k;
+      lane_code_coords(lane, p, h, &row, &k);
+      const long long n = rt * kTileRows + row;
+      const int c = n < N ? codes[n * K + static_cast<long long>(g) * kGroup + k] : 0;
+      u[2 * p + h] = static_cast<uint32_t>(c + (1 << (BITS - 1)));
+    }
+  }
+  uint32_t w[BITS];
+  encode_lane(BITS, u, w);
+  uint8_t* base = packed + blk * block_bytes(BITS);
+#pragma unroll
+  for (int i = 0; i < BITS; ++i)
+    *reinterpret_cast<uint32_t*>(base + lane_word_offset(BITS, lane, i)) = w[i];
+  if (lane < 16) {
+    const int m = lane & 7, h = lane >> 3;
+    const long long n = rt * kTileRows + lane;
+    scales_out[blk * 16 + 2 * m + h] = n < N ? scales[n * G + g] : static_cast<uint16_t>(0);
+  }
+}
+
+cudaError_t launch_pack_device(const int8_t* codes, const uint16_t* scales, long long K,
+                               long long N, int bits, void* packed, uint16_t* scales_out,
+                               cudaStream_t st) {
+  const int G = static_cast<int>(K / kGroup);
+  const long long nt = (N + kTileRows - 1) / kTileRows;
+  const long long nthreads = nt * G * 32;
+  const int block = 256;
+  const long long grid = (nthreads + block - 1) / block;
+  auto* out = static_cast<uint8_t*>(packed);
+  switch (bits) {
+    case 4: pack_kernel<4><<<grid, block, 0, st>>>(codes, scales, K, N, G, nthreads, out, scales_out); break;
+    case 5: pack_kernel<5><<<grid, block, 0, st>>>(codes, scales, K, N, G, nthreads, out, scales_out); break;
+    default: pack_kernel<6><<<grid, block, 0, st>>>(codes, scales, K, N, G, nthreads, out, scales_out); break;
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ dequant
+// w = fp32(scale) * fp32(code), exact; uses the GEMV's own decode of a lane.
+template <int BITS>
+__global__ void dequant_kernel(const uint8_t* __restrict__ packed,
+                               const uint16_t* __restrict__ scales, long long K, long long N,
+                               int G, long long nthreads, float* __restrict__ w) {
+  const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (tid >= nthreads) return;
+  const int lane = static_cast<int>(tid & 31);
+  const long long blk = tid >> 5;
+  const long long rt = blk / G;
+  const int g = static_cast<int>(blk - rt * G);
+  const uint8_t* base = packed + blk * block_bytes(BITS);
+  uint32_t words[BITS];
+#pragma unroll
+  for (int i = 0; i < BITS; ++i)
+    words[i] = *reinterpret_cast<const uint32_t*>(base + lane_word_offset(BITS, lane, i));
+#pragma unroll
+  for (int p = 0; p < 16; ++p) {
+    const uint32_t c2 = pair_codes_bf16<BITS>(words, p);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      int row, k;
+      lane_code_coords(lane, p, h, &row, &k);
+      const long long n = rt * kTileRows + row;
+      if (n >= N) continue;
+      const float c = __uint_as_float(h == 0 ? (c2 << 16) : (c2 & 0xFFFF0000u));
+      const uint16_t sb = scales[blk * 16 + 2 * (row & 7) + (row >> 3)];
+      const float s = __half2float(__ushort_as_half(sb));
+      w[n * K + static_cast<long long>(g) * kGroup + k] = s * c;
+    }
+  }
+}
+
+cudaError_t launch_dequant(const void* packed, const uint16_t* scales, float* w, long long K,
+                           long long N, int bits, cudaStream_t st) {
+  const int G = static_cast<int>(K / kGroup);
+  const long long nt = (N + kTileRows - 1) / kTileRows;
+  const long long nthreads = nt * G * 32;
+  const int block = 256;
+  const long long grid = (nthreads + block - 1) / block;
+  auto* in = static_cast<const uint8_t*>(packed);
+  switch (bits) {
+    case 4: dequant_kernel<4><<<grid, block, 0, st>>>(in, scales, K, N, G, nthreads, w); break;
+    case 5: dequant_kernel<5><<<grid, block, 0, st>>>(in, scales, K, N, G, nthreads, w); break;
+    default: dequant_kernel<6><<<grid, block, 0, st>>>(in, scales, K, N, G, nthreads, w); break;
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ RTN encoder
+// One warp per 64-group: absmax by warp reduction (exact), scale = FP16
+// round-to-nearest-even of the fp64 quotient absmax / qmax, codes
+// = clamp(rint(w / s)) with the quotient in fp64 (IEEE, correctly rounded).
+__global__ void quantize_rtn_kernel(const float* __restrict__ w, long long K, long long ngroups,
+                                    int G, int bits, int8_t* __restrict__ codes,
+                                    uint16_t* __restrict__ scales, int* status) {
+  const long long gw = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= ngroups) return;
+  const long long n = gw / G;
+  const int g = static_cast<int>(gw - n * G);
+  const long long off = n * K + static_cast<long long>(g) * kGroup + 2 * lane;
+  const float2 v = *reinterpret_cast<const float2*>(w + off);
+  float a = fmaxf(fabsf(v.x), fabsf(v.y));
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
+  const int qmax = (1 << (bits - 1)) - 1;
+  const __half sh = __double2half(static_cast<double>(a) / static_cast<double>(qmax));
+  const uint16_t sbits = __half_as_ushort(sh);
+  if ((sbits & 0x7C00u) == 0x7C00u) {
+    if (lane == 0) atomicCAS(status, 0, -3);
+  }
+  const double s = static_cast<double>(__half2float(sh));
+  int c0 = 0, c1 = 0;
+  if (s != 0.0) {
+    const double lo = -static_cast<double>(qmax) - 1.0, hi = static_cast<double>(qmax);
+    c0 = static_cast<int>(fmin(fmax(rint(static_cast<double>(v.x) / s), lo), hi));
+    c1 = static_cast<int>(fmin(fmax(rint(static_cast<double>(v.y) / s), lo), hi));
+  }
+  char2 cc;
+  cc.x = static_cast<signed char>(c0);
+  cc.y = static_cast<signed char>(c1);
+  *reinterpret_cast<char2*>(codes + off) = cc;
+  if (lane == 0) scales[n * G + g] = sbits;
+}
+
+cudaError_t launch_quantize_rtn(const float* w, long long K, long long N, int bits, int8_t* codes,
+                                uint16_t* scales, int* status, cudaStream_t st) {
+  const int G = static_cast<int>(K / kGroup);
+  const long long ngroups = N * G;
+  const int block = 256;  // 8 groups per block
+  const long long grid = (ngroups * 32 + block - 1) / block;
+  quantize_rtn_kernel<<<grid, block, 0, st>>>(w, K, ngroups, G, bits, codes, scales, status);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ self-test
+// Waits on a barrier that nothing completes; the bounded wait gives up after
+// `limit_ns`, records NQ_ETIMEOUT and the kernel returns normally.
+__global__ void selftest_timeout_kernel(unsigned long long limit_ns, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_addr(&bar), 1);
+  abort_flag = 0;
+  fence_mbar_init();
+  const Waiter wt{&abort_flag, limit_ns, status};
+  (void)wt.wait<false>(smem_addr(&bar), 0);
+}
+
+cudaError_t launch_selftest_timeout(unsigned long long limit_ns, int* status, cudaStream_t st) {
+  selftest_timeout_kernel<<<1, 32, 0, st>>>(limit_ns, status);
+  return cudaGetLastError();
+}
+
+}  // namespace nq

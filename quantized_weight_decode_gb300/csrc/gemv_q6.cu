@@ -1,0 +1,14 @@
+// Kernel instances of the groupwise GEMV for 6-bit codes.
+#include "gemv.cuh"
+
+namespace nq {
+
+const void* gemv_kernel_q6(int route, int ntok) {
+  if (route == kRouteMma) {
+    return ntok == 1 ? reinterpret_cast<const void*>(&gemv_kernel<6, kRouteMma, 1>)
+                     : reinterpret_cast<const void*>(&gemv_kernel<6, kRouteMma, 2>);
+  }
+  return reinterpret_cast<const void*>(&gemv_kernel<6, kRouteFfma, 4>);
+}
+
+}  // namespace nq

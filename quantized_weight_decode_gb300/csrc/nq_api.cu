@@ -1,0 +1,547 @@
+// Host side of the C ABI declared in include/nq.h: argument validation, the
+// host packer, launch planning and kernel launches.  Every step of the
+// computation runs in the kernels of gemv_q*.cu and aux_kernels.cu.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "gemv.cuh"
+#include "layout.h"
+#include "nq.h"
+
+namespace nq {
+const void* gemv_kernel_q4(int route, int ntok);
+const void* gemv_kernel_q5(int route, int ntok);
+const void* gemv_kernel_q6(int route, int ntok);
+cudaError_t launch_pack_device(const int8_t*, const uint16_t*, long long, long long, int, void*,
+                               uint16_t*, cudaStream_t);
+cudaError_t launch_dequant(const void*, const uint16_t*, float*, long long, long long, int,
+                           cudaStream_t);
+cudaError_t launch_quantize_rtn(const float*, long long, long long, int, int8_t*, uint16_t*, int*,
+                                cudaStream_t);
+cudaError_t launch_selftest_timeout(unsigned long long, int*, cudaStream_t);
+int* device_status_ptr();
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxT = 16;
+constexpr int kFfmaMaxT = 4;
+
+struct DevInfo {
+  bool ready = false;
+  int sms = 0;
+  int smem_optin = 0;
+  int* status = nullptr;
+};
+
+std::mutex g_mu;
+DevInfo g_dev[kMaxDevices];
+std::map<std::tuple<int, const void*>, bool> g_func_ready;
+std::map<std::tuple<int, const void*, int, int>, int> g_clusters;
+
+int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return NQ_ECUDA;
+  }
+  if (*dev < 0 || *dev >= kMaxDevices) return NQ_ECUDA;
+  return NQ_OK;
+}
+
+int dev_info(DevInfo** out) {
+  int dev;
+  if (int rc = current_device(&dev)) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess) {
+      (void)cudaGetLastError();
+      return NQ_ECUDA;
+    }
+    d.status = device_status_ptr();
+    if (!d.status) {
+      (void)cudaGetLastError();
+      return NQ_ECUDA;
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return NQ_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int64_t K, int64_t N, int bits) {
+  if (K <= 0 || N <= 0 || K % kGroup != 0) return NQ_EINVAL;
+  if (bits < 4 || bits > 6) return NQ_EINVAL;
+  if (K / kGroup > (1LL << 30) || N > (1LL << 40)) return NQ_EINVAL;
+  return NQ_OK;
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  return std::atoi(v);
+}
+
+int env_route() {
+  const char* v = std::getenv("NQ_ROUTE");
+  if (!v || !*v) return NQ_ROUTE_AUTO;
+  if (!std::strcmp(v, "mma")) return NQ_ROUTE_MMA;
+  if (!std::strcmp(v, "ffma")) return NQ_ROUTE_FFMA;
+  return NQ_ROUTE_AUTO;
+}
+
+const void* kernel_for(int bits, int route, int ntok) {
+  switch (bits) {
+    case 4: return gemv_kernel_q4(route, ntok);
+    case 5: return gemv_kernel_q5(route, ntok);
+    default: return gemv_kernel_q6(route, ntok);
+  }
+}
+
+int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+struct Plan {
+  int route = 0, ntok = 0, ks = 1, clusters = 0, sg = 16, stages = 0, stage_bytes = 0;
+  int smem = 0, off_stage = 0, off_red = 0, off_cl = 0, off_x = 0;
+  const void* func = nullptr;
+  double est_us = 0;
+};
+
+// Shared-memory layout for a K-split; false if it does not fit.
+bool layout_for(const Plan& base, int G, int T, int bits, int ks, int sg, int smem_optin,
+                Plan* out) {
+  Plan p = base;
+  p.ks = ks;
+  p.sg = sg;
+  const int gc_max = (G + ks - 1) / ks;
+  const long long x_bytes = 1LL * gc_max * T * (p.route == NQ_ROUTE_MMA ? 128 : 256);
+  const int red_bytes = 2 * kConsumerWarps * 16 * T * 4;
+  const int cl_bytes = ks > 1 ? 2 * (ks - 1) * 16 * T * 4 : 0;
+  p.stage_bytes = align_up(sg * (block_bytes(bits) + kScaleBytesPerBlock), 128);
+  p.off_red = kBarRegionBytes;
+  p.off_cl = p.off_red + align_up(red_bytes, 128);
+  p.off_x = p.off_cl + align_up(cl_bytes, 128);
+  const long long fixed = p.off_x + align_up(static_cast<int>(std::min<long long>(x_bytes, 1 << 30)), 128);
+  if (fixed >= smem_optin) return false;
+  p.off_stage = static_cast<int>(fixed);
+  const long long room = smem_optin - fixed;
+  p.stages = static_cast<int>(std::min<long long>(kMaxStages, room / p.stage_bytes));
+  if (p.stages < 2) return false;
+  p.smem = p.off_stage + p.stages * p.stage_bytes;
+  *out = p;
+  return true;
+}
+
+int prepare_func(int dev, const void* func, int smem_optin) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto key = std::make_tuple(dev, func);
+  if (g_func_ready.count(key)) return NQ_OK;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) !=
+      cudaSuccess) {
+    (void)cudaGetLastError();
+    return NQ_ECUDA;
+  }
+  g_func_ready[key] = true;
+  return NQ_OK;
+}
+
+// Clusters of `ks` CTAs (one CTA per SM) that can be resident at once.
+int max_clusters(int dev, const DevInfo& d, const void* func, int ks, int smem) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_clusters.find(std::make_tuple(dev, func, ks, smem));
+    if (it != g_clusters.end()) return it->second;
+  }
+  int n = 0;
+  if (ks == 1) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, kThreads, smem) != cudaSuccess)
+      per_sm = 1;
+    n = std::max(1, per_sm) * d.sms;
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ks * std::max(1, d.sms / ks));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = ks;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = d.sms / ks;
+    }
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_clusters[std::make_tuple(dev, func, ks, smem)] = n;
+  return n;
+}
+
+// Rough time model: the weight stream at the HBM rate while every SM is busy,
+// the last partial wave at the per-SM rate of the SMs that still have work.
+double estimate_us(const Plan& p, long long Nt, int G, int bits) {
+  const double bw = 6.5e12, bw_sm = 1.1e11;
+  const int gc_max = (G + p.ks - 1) / p.ks;
+  const double job_bytes = 1.0 * gc_max * (block_bytes(bits) + kScaleBytesPerBlock);
+  const long long C = p.clusters;
+  const long long rounds = Nt / C, rem = Nt % C;
+  const double act = static_cast<double>(C) * p.ks;
+  double t = rounds * act * job_bytes / std::min(bw, act * bw_sm);
+  if (rem) {
+    const double ract = static_cast<double>(rem) * p.ks;
+    t += ract * job_bytes / std::min(bw, ract * bw_sm);
+  }
+  t *= 1e6;
+  t += (p.ks > 1 ? 0.5 : 0.0);
+  return t;
+}
+
+int make_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, Plan* out) {
+  if (int rc = check_shape(K, N, bits)) return rc;
+  if (T < 1 || T > kMaxT) return NQ_EINVAL;
+  if (route == NQ_ROUTE_AUTO) route = env_route();
+  if (route == NQ_ROUTE_AUTO) route = NQ_ROUTE_MMA;
+  if (route != NQ_ROUTE_MMA && route != NQ_ROUTE_FFMA) return NQ_EINVAL;
+  if (route == NQ_ROUTE_FFMA && T > kFfmaMaxT) return NQ_EINVAL;
+  if (ksplit == 0) ksplit = env_int("NQ_KSPLIT", 0);
+  if (ksplit != 0 && ksplit != 1 && ksplit != 2 && ksplit != 4 && ksplit != 8) return NQ_EINVAL;
+
+  DevInfo* d;
+  if (int rc = dev_info(&d)) return rc;
+  int dev;
+  if (int rc = current_device(&dev)) return rc;
+
+  Plan base;
+  base.route = route;
+  base.ntok = route == NQ_ROUTE_MMA ? (T <= 8 ? 1 : 2) : kFfmaMaxT;
+  base.func = kernel_for(bits, route, base.ntok);
+  if (int rc = prepare_func(dev, base.func, d->smem_optin)) return rc;
+
+  const int G = static_cast<int>(K / kGroup);
+  const long long Nt = (N + kTileRows - 1) / kTileRows;
+  const int cands[4] = {1, 2, 4, 8};
+  bool have = false;
+  Plan best;
+  for (int ks : cands) {
+    if (ksplit != 0 && ks != ksplit) continue;
+    if (ks > G) continue;
+    Plan p;
+    bool fit = layout_for(base, G, T, bits, ks, 16, d->smem_optin, &p);
+    if (fit && p.stages < 4) {
+      Plan q;
+      if (layout_for(base, G, T, bits, ks, 8, d->smem_optin, &q) && q.stages > p.stages) p = q;
+    }
+    if (!fit && !layout_for(base, G, T, bits, ks, 8, d->smem_optin, &p)) continue;
+    const int mc = max_clusters(dev, *d, p.func, ks, p.smem);
+    if (mc <= 0) continue;
+    p.clusters = static_cast<int>(std::min<long long>(mc, Nt));
+    p.est_us = estimate_us(p, Nt, G, bits);
+    if (!have || p.est_us < best.est_us - 1e-3) {
+      best = p;
+      have = true;
+    }
+  }
+  if (!have) return NQ_EUNSUPPORTED;
+  *out = best;
+  return NQ_OK;
+}
+
+int launch_plan(const Plan& p, const void* packed, const uint16_t* scales, const void* x, float* y,
+                int64_t K, int64_t N, int T, cudaStream_t st) {
+  DevInfo* d;
+  if (int rc = dev_info(&d)) return rc;
+  GemvArgs a;
+  a.codes = static_cast<const uint8_t*>(packed);
+  a.scales = scales;
+  a.x = static_cast<const uint16_t*>(x);
+  a.y = y;
+  a.N = N;
+  a.K = static_cast<int>(K);
+  a.T = T;
+  a.G = static_cast<int>(K / kGroup);
+  a.Nt = static_cast<int>((N + kTileRows - 1) / kTileRows);
+  a.ksplit = p.ks;
+  a.clusters = p.clusters;
+  a.stage_groups = p.sg;
+  a.stages = p.stages;
+  a.stage_bytes = p.stage_bytes;
+  a.off_stage = p.off_stage;
+  a.off_red = p.off_red;
+  a.off_cl = p.off_cl;
+  a.off_x = p.off_x;
+  a.wait_ns = static_cast<unsigned long long>(std::max(1, env_int("NQ_WAIT_MS", 2000))) * 1000000ULL;
+  a.status = d->status;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.clusters * p.ks));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(p.smem);
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  int na = 0;
+  if (p.ks > 1) {
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = p.ks;
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (env_int("NQ_PDL", 1) != 0) {
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = na;
+  void* args[] = {&a};
+  if (cudaLaunchKernelExC(&cfg, p.func, args) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return NQ_ECUDA;
+  }
+  return NQ_OK;
+}
+
+template <int BITS>
+void pack_host(const int8_t* codes, const uint16_t* scales, int64_t K, int64_t N, uint8_t* out,
+               uint16_t* sout) {
+  const int64_t G = K / kGroup, Nt = (N + kTileRows - 1) / kTileRows;
+  constexpr uint32_t bias = 1u << (BITS - 1);
+  for (int64_t rt = 0; rt < Nt; ++rt) {
+    for (int64_t g = 0; g < G; ++g) {
+      const int64_t blk = rt * G + g;
+      uint8_t* base = out + blk * block_bytes(BITS);
+      for (int lane = 0; lane < kLanes; ++lane) {
+        uint32_t u[32], w[8];
+        for (int p = 0; p < 16; ++p) {
+          for (int h = 0; h < 2; ++h) {
+            int row, k;
+            lane_code_coords(lane, p, h, &row, &k);
+            const int64_t n = rt * kTileRows + row;
+            const int c = n < N ? codes[n * K + g * kGroup + k] : 0;
+            u[2 * p + h] = static_cast<uint32_t>(c + static_cast<int>(bias));
+          }
+        }
+        encode_lane(BITS, u, w);
+        for (int i = 0; i < BITS; ++i) {
+          std::memcpy(base + lane_word_offset(BITS, lane, i), &w[i], 4);
+        }
+      }
+      for (int row = 0; row < kTileRows; ++row) {
+        const int64_t n = rt * kTileRows + row;
+        sout[blk * 16 + 2 * (row & 7) + (row >> 3)] = n < N ? scales[n * G + g] : 0;
+      }
+    }
+  }
+}
+
+template <int BITS>
+void unpack_host(const uint8_t* in, const uint16_t* sin, int64_t K, int64_t N, int8_t* codes,
+                 uint16_t* scales) {
+  const int64_t G = K / kGroup, Nt = (N + kTileRows - 1) / kTileRows;
+  constexpr int bias = 1 << (BITS - 1);
+  constexpr uint32_t mask = (1u << BITS) - 1;
+  for (int64_t rt = 0; rt < Nt; ++rt) {
+    for (int64_t g = 0; g < G; ++g) {
+      const int64_t blk = rt * G + g;
+      const uint8_t* base = in + blk * block_bytes(BITS);
+      for (int lane = 0; lane < kLanes; ++lane) {
+        uint32_t w[BITS];
+        for (int i = 0; i < BITS; ++i) std::memcpy(&w[i], base + lane_word_offset(BITS, lane, i), 4);
+        for (int p = 0; p < 16; ++p) {
+          const uint32_t f = pair_field<BITS>(w, p);
+          for (int h = 0; h < 2; ++h) {
+            int row, k;
+            lane_code_coords(lane, p, h, &row, &k);
+            const int64_t n = rt * kTileRows + row;
+            if (n >= N) continue;
+            codes[n * K + g * kGroup + k] =
+                static_cast<int8_t>(static_cast<int>((f >> (16 * h)) & mask) - bias);
+          }
+        }
+      }
+      for (int row = 0; row < kTileRows; ++row) {
+        const int64_t n = rt * kTileRows + row;
+        if (n < N) scales[n * G + g] = sin[blk * 16 + 2 * (row & 7) + (row >> 3)];
+      }
+    }
+  }
+}
+
+}  // namespace
+}  // namespace nq
+
+using namespace nq;
+
+extern "C" {
+
+const char* nq_status_string(int status) {
+  switch (status) {
+    case NQ_OK: return "ok";
+    case NQ_EINVAL: return "invalid argument (size, width, T, route or null pointer)";
+    case NQ_EALIGN: return "device pointer not 16-byte aligned";
+    case NQ_ERANGE: return "code out of range or scale not finite / overflowing FP16";
+    case NQ_ECUDA: return "CUDA error";
+    case NQ_ETIMEOUT: return "a kernel's bounded wait gave up";
+    case NQ_EUNSUPPORTED: return "shape does not fit the shared-memory x tile";
+    default: return "unknown status";
+  }
+}
+
+int nq_layout_version(void) { return kLayoutVersion; }
+
+int nq_packed_bytes(int64_t K, int64_t N, int bits, size_t* codes_bytes, size_t* scales_bytes) {
+  if (int rc = check_shape(K, N, bits)) return rc;
+  const int64_t G = K / kGroup, Nt = (N + kTileRows - 1) / kTileRows;
+  if (codes_bytes) *codes_bytes = static_cast<size_t>(Nt * G * block_bytes(bits));
+  if (scales_bytes) *scales_bytes = static_cast<size_t>(Nt * G * kScaleBytesPerBlock);
+  return NQ_OK;
+}
+
+int nq_pack(const int8_t* codes, const uint16_t* scales, int64_t K, int64_t N, int bits,
+            void* packed_out, uint16_t* scales_out) {
+  if (int rc = check_shape(K, N, bits)) return rc;
+  if (!codes || !scales || !packed_out || !scales_out) return NQ_EINVAL;
+  const int lo = -(1 << (bits - 1)), hi = (1 << (bits - 1)) - 1;
+  const int64_t total = K * N;
+  for (int64_t i = 0; i < total; ++i)
+    if (codes[i] < lo || codes[i] > hi) return NQ_ERANGE;
+  const int64_t ns = N * (K / kGroup);
+  for (int64_t i = 0; i < ns; ++i)
+    if ((scales[i] & 0x7C00u) == 0x7C00u) return NQ_ERANGE;
+  auto* out = static_cast<uint8_t*>(packed_out);
+  switch (bits) {
+    case 4: pack_host<4>(codes, scales, K, N, out, scales_out); break;
+    case 5: pack_host<5>(codes, scales, K, N, out, scales_out); break;
+    default: pack_host<6>(codes, scales, K, N, out, scales_out); break;
+  }
+  return NQ_OK;
+}
+
+int nq_unpack(const void* packed, const uint16_t* scales_packed, int64_t K, int64_t N, int bits,
+              int8_t* codes_out, uint16_t* scales_out) {
+  if (int rc = check_shape(K, N, bits)) return rc;
+  if (!packed || !scales_packed || !codes_out || !scales_out) return NQ_EINVAL;
+  auto* in = static_cast<const uint8_t*>(packed);
+  switch (bits) {
+    case 4: unpack_host<4>(in, scales_packed, K, N, codes_out, scales_out); break;
+    case 5: unpack_host<5>(in, scales_packed, K, N, codes_out, scales_out); break;
+    default: unpack_host<6>(in, scales_packed, K, N, codes_out, scales_out); break;
+  }
+  return NQ_OK;
+}
+
+int nq_pack_device(const int8_t* codes, const uint16_t* scales, int64_t K, int64_t N, int bits,
+                   void* packed_out, uint16_t* scales_out, nq_stream_t stream) {
+  if (int rc = check_shape(K, N, bits)) return rc;
+  if (!codes || !scales || !packed_out || !scales_out) return NQ_EINVAL;
+  if (!aligned16(codes) || !aligned16(packed_out) || !aligned16(scales_out)) return NQ_EALIGN;
+  if (launch_pack_device(codes, scales, K, N, bits, packed_out, scales_out,
+                         reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return NQ_ECUDA;
+  }
+  return NQ_OK;
+}
+
+int nq_quantize_rtn(const float* w, int64_t K, int64_t N, int bits, int8_t* codes_out,
+                    uint16_t* scales_out, nq_stream_t stream) {
+  if (int rc = check_shape(K, N, bits)) return rc;
+  if (!w || !codes_out || !scales_out) return NQ_EINVAL;
+  if (!aligned16(w) || !aligned16(codes_out)) return NQ_EALIGN;
+  DevInfo* d;
+  if (int rc = dev_info(&d)) return rc;
+  if (launch_quantize_rtn(w, K, N, bits, codes_out, scales_out, d->status,
+                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return NQ_ECUDA;
+  }
+  return NQ_OK;
+}
+
+int nq_gemv_ex(const void* packed, const uint16_t* scales, const void* x_bf16, float* y,
+               int64_t K, int64_t N, int T, int bits, int route, int ksplit, nq_stream_t stream) {
+  if (!packed || !scales || !x_bf16 || !y) return NQ_EINVAL;
+  if (int rc = check_shape(K, N, bits)) return rc;
+  if (T < 1 || T > kMaxT) return NQ_EINVAL;
+  if (!aligned16(packed) || !aligned16(scales) || !aligned16(x_bf16) || !aligned16(y))
+    return NQ_EALIGN;
+  Plan p;
+  if (int rc = make_plan(K, N, T, bits, route, ksplit, &p)) return rc;
+  return launch_plan(p, packed, scales, x_bf16, y, K, N, T, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int nq_gemv(const void* packed, const uint16_t* scales, const void* x_bf16, float* y, int64_t K,
+            int64_t N, int T, int bits, nq_stream_t stream) {
+  return nq_gemv_ex(packed, scales, x_bf16, y, K, N, T, bits, NQ_ROUTE_AUTO, 0, stream);
+}
+
+int nq_gemv_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, int* route_out,
+                 int* ksplit_out, int* clusters_out, int* stages_out, int* smem_out) {
+  Plan p;
+  if (int rc = make_plan(K, N, T, bits, route, ksplit, &p)) return rc;
+  if (route_out) *route_out = p.route;
+  if (ksplit_out) *ksplit_out = p.ks;
+  if (clusters_out) *clusters_out = p.clusters;
+  if (stages_out) *stages_out = p.stages;
+  if (smem_out) *smem_out = p.smem;
+  return NQ_OK;
+}
+
+int nq_dequant(const void* packed, const uint16_t* scales, float* w, int64_t K, int64_t N, int bits,
+               nq_stream_t stream) {
+  if (int rc = check_shape(K, N, bits)) return rc;
+  if (!packed || !scales || !w) return NQ_EINVAL;
+  if (!aligned16(packed) || !aligned16(scales) || !aligned16(w)) return NQ_EALIGN;
+  if (launch_dequant(packed, scales, w, K, N, bits, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess) {
+    (void)cudaGetLastError();
+    return NQ_ECUDA;
+  }
+  return NQ_OK;
+}
+
+int nq_last_device_error(nq_stream_t stream) {
+  DevInfo* d;
+  if (int rc = dev_info(&d)) return rc;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return NQ_ECUDA;
+  }
+  int v = 0;
+  const int zero = 0;
+  if (cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return NQ_ECUDA;
+  }
+  return v;
+}
+
+int nq_selftest_wait_timeout(int limit_us, nq_stream_t stream) {
+  if (limit_us <= 0 || limit_us > 10000000) return NQ_EINVAL;
+  DevInfo* d;
+  if (int rc = dev_info(&d)) return rc;
+  if (launch_selftest_timeout(static_cast<unsigned long long>(limit_us) * 1000ULL, d->status,
+                              reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return NQ_ECUDA;
+  }
+  return NQ_OK;
+}
+
+}  // extern "C"

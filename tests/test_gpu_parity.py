@@ -1,0 +1,292 @@
+"""GPU parity of the CUDA path against the CPU oracle, through the C ABI.
+
+Bar: bit-exact for the encoder (codes, scale bits), the packers and the
+dequantised weights; |y - y*| <= 1e-4 * sum|w x| + 1e-6 per output for the
+GEMV (the tolerance of oracle.tolerance_ok); exact equality where the
+arithmetic is provably identical (one-hot inputs, zero codes, negated scales,
+T-invariance at a fixed launch plan, repeat runs)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_weight_decode_gb300 as nqp
+from cases import device_weight, device_x, oracle_inputs, rtn_case, uniform_case
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    nqp.build()
+    nqp.lib()
+    torch.cuda.set_device(0)
+    assert nqp.last_device_error() == 0
+
+
+def _y(case, packed, sp, route=0, ksplit=0, T=None):
+    T = case["T"] if T is None else T
+    x = device_x(torch, case, DEV)[:T].contiguous()
+    y = torch.full((T, case["N"]), float("nan"), dtype=torch.float32, device=DEV)
+    nqp.gemv(packed, sp, x, y, case["K"], case["N"], T, case["bits"], route=route, ksplit=ksplit)
+    assert nqp.last_device_error() == 0
+    return y.cpu().numpy()
+
+
+def _check(case, y, rows=None):
+    codes, sb = oracle_inputs(case, rows)
+    y_ref, e_ref = oracle.gemv(codes, sb, case["xb"][: y.shape[0]])
+    got = y if rows is None else y[:, rows]
+    v = oracle.max_violation(got, y_ref, e_ref)
+    assert v <= 1.0, f"tolerance ratio {v}"
+    return v
+
+
+# ---------------------------------------------------------------- encoder, packers, dequant
+@pytest.mark.parametrize("bits", [4, 5, 6])
+def test_quantize_rtn_bit_exact(bits):
+    case = rtn_case((300, bits), bits, 96, 512, 1)
+    w = case["w"]
+    w[0, :64] = 0                                    # all-zero group
+    w[1, :64] *= np.float32(1e-6)                    # subnormal-scale group
+    w[2, 64:128] = np.float32(0.5)                   # constant group
+    w[3, 128:192] *= np.float32(300.0)               # large magnitudes
+    codes, scales = nqp.quantize_rtn(torch.from_numpy(w).to(DEV), bits)
+    assert nqp.last_device_error() == 0
+    c_ref, s_ref = oracle.rtn_encode(w, bits)
+    assert np.array_equal(codes.cpu().numpy(), c_ref)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint16), s_ref)
+
+
+def test_quantize_rtn_overflow_sets_status():
+    w = torch.full((16, 64), 7.0 * 70000.0, dtype=torch.float32, device=DEV)
+    nqp.quantize_rtn(w, 4)
+    assert nqp.last_device_error() == nqp.ERANGE
+    assert nqp.last_device_error() == 0              # read clears
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6])
+def test_pack_device_matches_host_pack(bits):
+    case = uniform_case((301, bits), bits, 53, 320, 1)
+    codes, sb = oracle_inputs(case)
+    hp, hs = nqp.pack(codes, sb, bits)
+    dp, ds = nqp.pack_device(torch.from_numpy(codes).to(DEV),
+                             torch.from_numpy(sb.view(np.int16)).to(DEV), bits)
+    assert nqp.last_device_error() == 0
+    assert np.array_equal(dp.cpu().numpy(), hp)
+    assert np.array_equal(ds.cpu().numpy().view(np.uint16), hs)
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("kind", ["rtn", "uniform"])
+def test_dequant_bit_exact(bits, kind):
+    mk = rtn_case if kind == "rtn" else uniform_case
+    case = mk((302, bits), bits, 77, 384, 1)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    w = nqp.dequant(packed, sp, case["K"], case["N"], bits).cpu().numpy()
+    codes, sb = oracle_inputs(case)
+    ref = oracle.dequant_f32(codes, sb)
+    assert np.array_equal(w.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6])
+def test_dequant_every_scale_pattern(bits):
+    # all 63,488 finite FP16 scale patterns x codes cycling through the range
+    finite = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    finite = finite[(finite & 0x7C00) != 0x7C00]
+    G = 8
+    N = -(-finite.size // G)
+    sb = np.zeros(N * G, np.uint16)
+    sb[: finite.size] = finite
+    sb = sb.reshape(N, G)
+    lo, hi = oracle.code_range(bits)
+    codes = (lo + (np.arange(N * G * 64) % (hi - lo + 1))).astype(np.int8).reshape(N, G * 64)
+    hp, hs = nqp.pack(codes, sb, bits)
+    w = nqp.dequant(torch.from_numpy(hp).to(DEV), torch.from_numpy(hs.view(np.int16)).to(DEV),
+                    G * 64, N, bits).cpu().numpy()
+    ref = oracle.dequant_f32(codes, sb)
+    assert np.array_equal(w.view(np.uint32), ref.view(np.uint32))
+
+
+# ---------------------------------------------------------------- GEMV parity
+SHAPES = [(512, 256), (1024, 200), (2048, 37), (64, 16), (192, 1)]
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("T", [1, 2, 3, 8, 9, 16])
+def test_gemv_mma_parity(bits, T):
+    for i, (K, N) in enumerate(SHAPES):
+        case = uniform_case((303, bits, T, i), bits, N, K, T) if i % 2 else \
+            rtn_case((303, bits, T, i), bits, N, K, T)
+        packed, sp = device_weight(nqp, torch, case, DEV)
+        _check(case, _y(case, packed, sp, route=nqp.ROUTE_MMA))
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("T", [1, 2, 4])
+def test_gemv_ffma_parity(bits, T):
+    for i, (K, N) in enumerate(SHAPES[:3]):
+        case = uniform_case((304, bits, T, i), bits, N, K, T)
+        packed, sp = device_weight(nqp, torch, case, DEV)
+        _check(case, _y(case, packed, sp, route=nqp.ROUTE_FFMA))
+
+
+@pytest.mark.parametrize("ksplit", [1, 2, 4, 8])
+@pytest.mark.parametrize("T", [1, 8, 16])
+def test_gemv_ksplit_parity(ksplit, T):
+    case = uniform_case((305, ksplit, T), 5, 300, 17408 // 8, T)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    _check(case, _y(case, packed, sp, route=nqp.ROUTE_MMA, ksplit=ksplit))
+
+
+def test_tiny_config():
+    case = rtn_case((1,), 4, 256, 512, 1)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    _check(case, _y(case, packed, sp))
+
+
+def test_many_jobs_per_cluster():
+    # more row tiles than resident clusters: every CTA runs several jobs and
+    # the reduction slots wrap around many times
+    case = rtn_case((306,), 6, 16 * 700 + 5, 256, 3)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    for ks in (1, 2):
+        _check(case, _y(case, packed, sp, route=nqp.ROUTE_MMA, ksplit=ks))
+
+
+# ---------------------------------------------------------------- exact invariants
+def _upload_packed(codes, sb, bits):
+    hp, hs = nqp.pack(codes, sb, bits)
+    return torch.from_numpy(hp).to(DEV), torch.from_numpy(hs.view(np.int16)).to(DEV)
+
+
+@pytest.mark.parametrize("bits", [4, 6])
+def test_one_hot_x_gives_weight_column_exactly(bits):
+    case = uniform_case((307, bits), bits, 100, 1024, 4)
+    codes, sb = oracle_inputs(case)
+    packed, sp = _upload_packed(codes, sb, bits)
+    ks_cols = [0, 63, 64, 517, 1023]
+    xb = np.zeros((len(ks_cols), 1024), np.uint16)
+    for t, k in enumerate(ks_cols):
+        xb[t, k] = 0x3F80
+    c2 = dict(case, xb=xb, T=len(ks_cols))
+    for route, ks in ((nqp.ROUTE_MMA, 1), (nqp.ROUTE_MMA, 4), (nqp.ROUTE_FFMA, 2)):
+        y = _y(c2, packed, sp, route=route, ksplit=ks, T=4)
+        wref = oracle.dequant_f32(codes, sb)
+        for t in range(4):
+            assert np.array_equal(y[t], wref[:, ks_cols[t]]), (route, ks, t)
+
+
+def test_zero_codes_and_negated_scales():
+    case = uniform_case((308,), 5, 80, 512, 8)
+    codes, sb = oracle_inputs(case)
+    packed, sp = _upload_packed(np.zeros_like(codes), sb, 5)
+    assert np.all(_y(case, packed, sp) == 0)
+    p1, s1 = _upload_packed(codes, sb, 5)
+    p2, s2 = _upload_packed(codes, sb ^ np.uint16(0x8000), 5)
+    for route in (nqp.ROUTE_MMA, nqp.ROUTE_FFMA):
+        y1 = _y(case, p1, s1, route=route, ksplit=2, T=4)
+        y2 = _y(case, p2, s2, route=route, ksplit=2, T=4)
+        assert np.array_equal(y1, -y2)
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6])
+def test_t_invariance_exact(bits):
+    case = rtn_case((309, bits), bits, 150, 1024, 16)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    y16 = _y(case, packed, sp, route=nqp.ROUTE_MMA, ksplit=2, T=16)
+    for T in (1, 5, 8, 12):
+        yt = _y(case, packed, sp, route=nqp.ROUTE_MMA, ksplit=2, T=T)
+        assert np.array_equal(yt, y16[:T]), T
+    # a single-token call on token 11 alone equals row 11
+    c1 = dict(case, xb=case["xb"][11:12].copy(), T=1)
+    y1 = _y(c1, packed, sp, route=nqp.ROUTE_MMA, ksplit=2)
+    assert np.array_equal(y1[0], y16[11])
+
+
+def test_repeat_runs_identical():
+    case = uniform_case((310,), 5, 1000, 4096, 8)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    a = _y(case, packed, sp)
+    b = _y(case, packed, sp)
+    assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------- errors and edge cases
+def test_invalid_arguments():
+    case = rtn_case((311,), 4, 32, 128, 2)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    x = device_x(torch, case, DEV)
+    y = torch.empty((2, 32), dtype=torch.float32, device=DEV)
+    bad = [dict(T=0), dict(T=17), dict(route=nqp.ROUTE_FFMA, T=5), dict(ksplit=3), dict(route=9),
+           dict(K=100), dict(bits=7)]
+    for kw in bad:
+        args = dict(K=128, N=32, T=2, bits=4, route=0, ksplit=0)
+        args.update(kw)
+        with pytest.raises(nqp.NQError) as e:
+            nqp.gemv(packed, sp, x, y, args["K"], args["N"], args["T"], args["bits"],
+                     route=args["route"], ksplit=args["ksplit"])
+        assert e.value.code == nqp.EINVAL, kw
+    xbuf = torch.zeros(2 * 128 + 8, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(nqp.NQError) as e:
+        nqp.gemv(packed, sp, xbuf[1:], y, 128, 32, 2, 4)
+    assert e.value.code == nqp.EALIGN
+    with pytest.raises(nqp.NQError) as e:
+        nqp.plan(262144, 64, 16, 4)
+    assert e.value.code == nqp.EUNSUPPORTED
+    assert nqp.last_device_error() == 0
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    nqp.selftest_wait_timeout(50_000)
+    assert nqp.last_device_error() == nqp.ETIMEOUT
+    case = rtn_case((312,), 4, 64, 256, 1)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    _check(case, _y(case, packed, sp))
+
+
+def test_max_t_long_k():
+    case = uniform_case((313,), 5, 96, 17408, 16)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    p = nqp.plan(17408, 96, 16, 5)
+    assert p["ksplit"] >= 4
+    _check(case, _y(case, packed, sp))
+
+
+# ---------------------------------------------------------------- full-size shapes, sampled rows
+FULL = [
+    ("gate_up_q4", "rtn", 4, 34816, 5120, [1], 0.0),
+    ("down_q5", "uniform", 5, 5120, 17408, [1, 8], 0.01),
+    ("head_q6", "rtn", 6, 248320, 5120, [1, 2, 4, 8], 0.0),
+]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,kind,bits,N,K,Ts,outl", FULL)
+def test_full_size_sampled(name, kind, bits, N, K, Ts, outl):
+    T = max(Ts)
+    mk = rtn_case if kind == "rtn" else uniform_case
+    case = mk((400, bits), bits, N, K, T, outlier_frac=outl)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    case_w = case.pop("w")
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([[0, 1, 15, 16, N // 2, N - 17, N - 1],
+                                     rng.choice(N, 384, replace=False)]))
+    case["w"] = case_w[rows]
+    sub = dict(case)
+    if kind == "uniform":
+        sub["flips"] = case["flips"][rows]
+        sub["codes"] = case["codes"][rows]
+    # dequant of the sampled rows is bit-exact
+    wd = nqp.dequant(packed, sp, K, N, bits)
+    codes, sb = oracle_inputs(sub)
+    assert np.array_equal(wd[torch.from_numpy(rows).to(DEV)].cpu().numpy().view(np.uint32),
+                          oracle.dequant_f32(codes, sb).view(np.uint32))
+    del wd
+    for t in Ts:
+        y = _y(case, packed, sp, T=t)
+        y_ref, e_ref = oracle.gemv(codes, sb, case["xb"][:t])
+        v = oracle.max_violation(y[:, rows], y_ref, e_ref)
+        assert v <= 1.0, (name, t, v)
+        assert np.isfinite(y).all()
