@@ -1,0 +1,453 @@
+#!/usr/bin/env python3
+"""Weight-stream benchmark of the groupwise-quantized small-T GEMV on GB300.
+
+Workload: the per-token MLP + head weight stream of a 64-layer Qwen3.8-27B-
+shaped model -- per layer a fused gate+up GEMV (4-bit, K=5120, N=34816) and a
+down GEMV (K=17408, N=5120; 5-bit for layers 0-35, 4-bit for 36-63), then the
+6-bit output head (K=5120, N=248320) -- run at T = 1, 8 and 16 tokens.
+Weights are seeded N(0, 0.02) draws encoded round-to-nearest on the device;
+x is seeded N(0, 1) in bf16.  A step is one pass over the whole stack at each
+T (3 x 129 GEMVs, 31.5 GB of packed weights), inputs resident in HBM.
+
+The GEMVs of a pass are independent (no activation between them), so each
+pass is grouped by tensor kind: the 64 gate+up GEMVs, the 64 down GEMVs, the
+head; each group is one CUDA graph, and CUDA events between the groups give
+the average launch duration of each kernel inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle (fp64)
+on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+# The CPU oracle is timed single-threaded; fix BLAS threads before numpy loads.
+import os
+
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HIDDEN, INTER, VOCAB, LAYERS = 5120, 17408, 248320, 64
+TS = (1, 8, 16)
+METRIC = "quantized GEMV weight-stream GB/s and % of GB300 HBM peak, T=1/8/16"
+UNIT = "GB/s"
+
+
+def stack_tensors():
+    """(kind, layer, bits, K, N) of every GEMV of one pass."""
+    out = []
+    for l in range(LAYERS):
+        out.append(("gate_up", l, 4, HIDDEN, 2 * INTER))
+    for l in range(LAYERS):
+        out.append(("down", l, 5 if l < 36 else 4, INTER, HIDDEN))
+    out.append(("head", 0, 6, HIDDEN, VOCAB))
+    return out
+
+
+def packed_bytes(bits, K, N):
+    """Algorithmic bytes of one weight stream: packed codes + FP16 scales."""
+    return N * K // 64 * (8 * bits + 2)
+
+
+PASS_BYTES = sum(packed_bytes(b, K, N) for (_, _, b, K, N) in stack_tensors())
+KIND_BYTES = {k: sum(packed_bytes(b, K, N) for (kk, _, b, K, N) in stack_tensors() if kk == k)
+              for k in ("gate_up", "down", "head")}
+CONFIG = {
+    "workload": "64-layer Qwen3.8-27B-shaped MLP+head weight stream: per layer gate+up Q4 "
+                "5120x34816 and down 17408x5120 (Q5 layers 0-35, Q4 36-63), then the Q6 head "
+                "5120x248320; T=1/8/16; group 64, FP16 scales",
+    "T": list(TS),
+    "weight_bytes_per_pass": PASS_BYTES,
+    "l2": "inputs larger than L2 (10.49 GB of distinct packed weights per pass, L2 129 MB)",
+    "launch": "one CUDA graph per tensor kind and T, programmatic dependent launch",
+}
+
+
+def source_hash() -> str:
+    """Hash of the kernel sources, to tell whether stored ncu counters still apply."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_weight_decode_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic():
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, or None if absent or taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "gemv_gate_up_q4_T1_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if "=" in line and not line.startswith("#"):
+                k, v = line.split("=", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("source_hash") != source_hash():
+        return None
+    try:
+        return int(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ("active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap")
+        reasons = set()
+        for _, _, flags in rows:
+            for n, f in zip(names[1:], flags[1:]):
+                if f.lower() in ("active", "1"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+def oracle_sample(seconds: float, seed: int = 77):
+    """Time the CPU oracle (fp64) on sampled rows of the same workload: rows of
+    the gate+up, down and head tensors at T = 1, 8, 16, in proportion to their
+    bytes.  Returns (GB/s of packed-weight bytes, bytes, seconds, description)."""
+    import oracle
+    import synth
+    rows = {"gate_up": (4, HIDDEN, 96), "down": (5, INTER, 16), "head": (6, HIDDEN, 64)}
+    prepared = []
+    for i, (kind, (bits, K, n)) in enumerate(rows.items()):
+        rng = synth.generator(seed, 700 + i)
+        w = synth.gauss_weights(rng, n, K)
+        codes, sb = oracle.rtn_encode(w, bits)
+        xs = {T: synth.gauss_x_bf16(rng, T, K) for T in TS}
+        prepared.append((kind, bits, K, n, codes, sb, xs))
+    done_bytes, t0, reps = 0, time.perf_counter(), 0
+    while True:
+        for (kind, bits, K, n, codes, sb, xs) in prepared:
+            for T in TS:
+                oracle.gemv(codes, sb, xs[T])
+                done_bytes += packed_bytes(bits, K, n)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    desc = (f"oracle.gemv (fp64, single thread) on {reps} rounds of sampled rows "
+            f"(gate+up 96 rows, down 16 rows, head 64 rows) at T=1,8,16")
+    return done_bytes / el / 1e9, done_bytes, el, desc
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    per_step = max(0.5, args.ref_step_seconds)
+    for _ in range(args.warmup):
+        oracle_sample(per_step / 4)
+    t0 = time.perf_counter()
+    total_bytes = 0
+    desc = ""
+    for _ in range(args.steps):
+        _, b, _, desc = oracle_sample(per_step)
+        total_bytes += b
+    el = time.perf_counter() - t0
+    value = total_bytes / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": CONFIG,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": desc + f"; {per_step:.1f} s per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU leg
+def build_stack(torch, nqp, dev, seed):
+    """Packed weights of every tensor, x arena (16 tokens per GEMV), y buffers."""
+    entries = []
+    for idx, (kind, layer, bits, K, N) in enumerate(stack_tensors()):
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed * 1000003 + idx)
+        w = torch.randn((N, K), generator=g, device=dev, dtype=torch.float32)
+        w.mul_(0.02)
+        qw = nqp.QuantizedWeight.from_fp32(w, bits)
+        del w
+        entries.append({"kind": kind, "layer": layer, "bits": bits, "K": K, "N": N, "qw": qw})
+    torch.cuda.synchronize()
+    rc = nqp.last_device_error()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} while preparing weights")
+    # x arena: 16 tokens per GEMV, seeded N(0,1) rounded to bf16
+    offs, tot = [], 0
+    for e in entries:
+        offs.append(tot)
+        tot += 16 * e["K"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed * 7919 + 1)
+    x_arena = torch.randn(tot, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    for e, o in zip(entries, offs):
+        e["x"] = x_arena[o:o + 16 * e["K"]].view(16, e["K"])
+    ys = {k: torch.empty((16, n), dtype=torch.float32, device=dev)
+          for k, n in (("gate_up", 2 * INTER), ("down", HIDDEN), ("head", VOCAB))}
+    return entries, x_arena, ys
+
+
+def capture(torch, nqp, entries, ys, T, kind, stream):
+    sel = [e for e in entries if e["kind"] == kind]
+
+    def run():
+        for e in sel:
+            nqp.gemv(e["qw"].packed, e["qw"].scales, e["x"][:T], ys[kind][:T], e["K"], e["N"], T,
+                     e["bits"], stream=stream)
+    with torch.cuda.stream(stream):
+        run()                                     # plans cached, attributes set
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run()
+    return g, len(sel)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import quantized_weight_decode_gb300 as nqp
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    nqp.build()
+    nqp.lib()
+    dist = world > 1
+    if dist:
+        import torch.distributed as td
+
+    def barrier():
+        if dist:
+            td.barrier()
+
+    entries, x_arena, ys = build_stack(torch, nqp, dev, seed=args.seed + rank)
+    stream = torch.cuda.Stream(device=dev)
+    kinds = ("gate_up", "down", "head")
+    graphs = {}
+    launches_per_pass = 0
+    for T in TS:
+        for k in kinds:
+            graphs[(T, k)], n = capture(torch, nqp, entries, ys, T, k, stream)
+            if T == TS[0]:
+                launches_per_pass += n
+    rc = nqp.last_device_error(stream)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} after capture")
+
+    def one_step(evs=None):
+        for T in TS:
+            for k in kinds:
+                graphs[(T, k)].replay()
+                if evs is not None:
+                    evs[(T, k)].append(torch.cuda.Event(enable_timing=True))
+                    evs[(T, k)][-1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            one_step()
+    stream.synchronize()
+
+    # ---------------- timed region
+    evs = {key: [] for key in graphs}
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(args.steps):
+            one_step(evs)
+        end.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    rc = nqp.last_device_error(stream)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} in timed region")
+    total_ms = start.elapsed_time(end)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        td.all_reduce(t, op=td.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # per-(T, kind) durations from consecutive events
+    seg = {key: 0.0 for key in graphs}
+    prev = start
+    for s in range(args.steps):
+        for T in TS:
+            for k in kinds:
+                e = evs[(T, k)][s]
+                seg[(T, k)] += prev.elapsed_time(e)
+                prev = e
+
+    # ---------------- end to end: x from pinned host, logits back to pinned host
+    x_host = torch.empty(x_arena.shape, dtype=x_arena.dtype, pin_memory=True)
+    x_host.copy_(x_arena)
+    y_host = {T: torch.empty((T, VOCAB), dtype=torch.float32, pin_memory=True) for T in TS}
+    h2d = x_arena.numel() * x_arena.element_size()
+    d2h = sum(T * VOCAB * 4 for T in TS)
+    e2e_steps = max(3, min(args.steps, 50))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            x_arena.copy_(x_host, non_blocking=True)
+            for T in TS:
+                for k in kinds:
+                    graphs[(T, k)].replay()
+                y_host[T].copy_(ys["head"][:T], non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        td.all_reduce(t, op=td.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    steps = args.steps
+    value = world * steps * len(TS) * PASS_BYTES / (total_ms * 1e-3) / 1e9
+    e2e_value = world * e2e_steps * len(TS) * PASS_BYTES / (e2e_ms * 1e-3) / 1e9
+    per_t = {}
+    for T in TS:
+        ms = sum(seg[(T, k)] for k in kinds) / steps
+        gbs = PASS_BYTES / (ms * 1e-3) / 1e9
+        per_t[str(T)] = {"us_per_pass": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                         "frac_of_measured_hbm": round(gbs / peak, 4),
+                         "frac_of_8tbs": round(gbs / 8000.0, 4)}
+    kernels = {}
+    for T in TS:
+        for k in kinds:
+            n = sum(1 for e in entries if e["kind"] == k)
+            us = seg[(T, k)] / steps / n * 1e3
+            gbs = KIND_BYTES[k] / n / (us * 1e-6) / 1e9
+            kernels[f"{k}_T{T}"] = {"us_per_launch": round(us, 2), "gbs": round(gbs, 1),
+                                    "frac": round(gbs / peak, 4)}
+    dom = kernels["gate_up_T1"]
+    roofline = {"bound": "hbm", "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
+                "frac": round(dom["gbs"] / peak, 4), "traffic": stored_traffic(),
+                "kernel": "gemv_kernel<4,MMA,1> gate+up Q4 K=5120 N=34816 T=1",
+                "bytes_per_launch": packed_bytes(4, HIDDEN, 2 * INTER),
+                "peak_source": peak_kind}
+    cpu_v, _, cpu_s, cpu_desc = oracle_sample(args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(CONFIG, parallelism=f"replicas x{world}"),
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": steps * len(TS) * launches_per_pass,
+        "roofline": roofline,
+        "cpu_baseline": {"value": round(cpu_v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": cpu_desc + f" for {cpu_s:.1f} s"},
+        "clocks": clocks,
+        "per_T": per_t,
+        "kernels": kernels,
+        "plans": {f"{k}_T{T}": nqp.plan(e["K"], e["N"], T, e["bits"])
+                  for T in TS for k in kinds
+                  for e in [next(x for x in entries if x["kind"] == k)]},
+        "source_hash": source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=2.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as td
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        td.init_process_group(backend=backend)
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as td
+        td.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
