@@ -10,27 +10,31 @@
 // leads" and "Engineering").  The kernel structure is our own design for one
 // GB300 SM:
 //
-//   warp 0..15 consumers : each owns a fixed K slice of the CTA's K range and
-//                          streams its own chunks (several 64-groups of one
-//                          16-row tile, plus their scales) with 1-D bulk copies
-//                          (TMA engine, L2 evict-first) into a private ring of
-//                          shared-memory slots; it decodes the codes in
-//                          registers, contracts them with the x tile (bf16 MMA
-//                          m16n8k16 or fp32 FMA) and scales each 64-wide
-//                          partial by the group's FP16 scale;
-//   warp 16    epilogue  : sums the 16 per-warp partials of a row tile in a
+//   warp 0..15 consumers : decode the codes of their groups in registers,
+//                          contract them with x (bf16 MMA m16n8k16, or fp32
+//                          FMA) and scale each 64-wide partial by the group's
+//                          FP16 scale;
+//   warp 16    producer  : one thread streams the weight stream in large
+//                          stages -- the CTA's whole K range of one 16-row
+//                          tile when it fits -- with two 1-D bulk copies per
+//                          stage (codes, scales; TMA engine, L2 evict-first)
+//                          into a ring of shared-memory stages;
+//   warp 17    epilogue  : sums the 16 per-warp partials of a row tile in a
 //                          fixed order, adds the partials of the other CTAs of
-//                          its cluster (K split, distributed shared memory,
-//                          rank order) and stores y.
+//                          its cluster (K split, asynchronous distributed
+//                          shared-memory stores, rank order) and stores y.
 //
-// A warp refills a ring slot as soon as it has read it, so no CTA-wide
-// handshake sits on the weight stream.  Work split: a persistent grid of
-// clusters of KS CTAs; cluster c owns a contiguous range of 16-row tiles
-// ("jobs"); rank q handles groups [q G / KS, (q+1) G / KS) of every job.  The
-// x slice of a CTA is loaded once into shared memory, permuted into MMA
-// B-fragment order.  Every wait is bounded by a time limit; on expiry the
-// kernel records NQ_ETIMEOUT in the status word and winds down without
-// hanging or leaving bulk copies in flight.
+// Few large copies matter: the bulk-copy engine of an SM serves a limited
+// number of requests per microsecond, so small per-warp copies cap the
+// stream well below the HBM rate.  Work split: a persistent grid of clusters
+// of KS CTAs; cluster c owns a contiguous range of 16-row tiles ("jobs");
+// rank q handles groups [q G / KS, (q+1) G / KS) of every job.  For T <= 8
+// each consumer warp owns a fixed slice of those groups and keeps its x
+// fragments in registers ("x in registers"); otherwise the CTA's x slice
+// sits in shared memory, permuted into B-fragment order, and the warps take
+// the groups of a stage in turn.  Every wait is bounded by a time limit; on
+// expiry the kernel records NQ_ETIMEOUT in the status word and winds down
+// without hanging or leaving bulk copies in flight.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -43,14 +47,15 @@
 namespace nq {
 
 constexpr int kWarps = 16;                   // consumer warps
-constexpr int kThreads = (kWarps + 1) * 32;  // + the epilogue warp
-constexpr int kEpilogueWarp = kWarps;
-constexpr int kMaxWarpStages = 8;            // ring slots per consumer warp
-constexpr int kMaxChunkGroups = 8;           // 64-groups per chunk
+constexpr int kProducerWarp = kWarps;
+constexpr int kEpilogueWarp = kWarps + 1;
+constexpr int kThreads = (kWarps + 2) * 32;
+constexpr int kMaxStages = 16;               // stages of the shared-memory ring
+constexpr int kMaxBufs = 8;                  // partial-sum buffers (warps -> epilogue, peers -> rank 0)
 constexpr int kStatusTimeout = -5;
-// MMA route kernel variants (template NTOK): 1 or 2 token blocks of 8 with x
-// in shared memory, or kNtokXreg: one token block, x in registers, at most
-// kXregMaxGroups groups per warp slice.
+// Kernel variants (template NTOK): MMA route with 1 or 2 token blocks of 8 and
+// x in shared memory, kNtokXreg (MMA, one token block, x in registers, at
+// most kXregMaxGroups groups per warp slice), FMA route: NTOK = max tokens.
 constexpr int kNtokXreg = 3;
 constexpr int kXregMaxGroups = 6;
 
@@ -65,27 +70,29 @@ struct GemvArgs {
   int K, T, G, Nt;
   int ksplit;              // CTAs per cluster splitting K
   int clusters;            // clusters in the grid
-  int chunk_groups;        // 64-groups per chunk (one pair of bulk copies)
-  int wstages;             // ring slots per consumer warp
-  int wstage_bytes;        // bytes of one slot (codes + scales, 128-aligned)
+  int stage_groups;        // 64-groups per stage (x in registers: the CTA's whole K range)
+  int stages;              // ring depth
+  int stage_bytes;         // bytes of one stage (codes, then scales; 128-aligned)
   int off_ring, off_red, off_cl, off_x;  // shared-memory offsets
+  int nbuf;                // partial-sum buffers in flight (<= kMaxBufs)
   unsigned long long wait_ns;
   int* status;
 };
 
-// Shared-memory map of the barrier region (first 2 KiB).
+// Shared-memory map of the barrier region (first 1 KiB).
 struct Bars {
   uint32_t base;
-  __device__ uint32_t full(int w, int s) const { return base + 8 * (w * kMaxWarpStages + s); }
-  __device__ uint32_t red_full(int b) const { return base + 1024 + 8 * b; }
-  __device__ uint32_t red_empty(int b) const { return base + 1040 + 8 * b; }
-  __device__ uint32_t cl_full(int b) const { return base + 1056 + 8 * b; }
-  __device__ uint32_t cl_empty(int b) const { return base + 1072 + 8 * b; }
+  __device__ uint32_t full(int s) const { return base + 8 * s; }
+  __device__ uint32_t empty(int s) const { return base + 8 * (kMaxStages + s); }
+  __device__ uint32_t red_full(int b) const { return base + 8 * (2 * kMaxStages + b); }
+  __device__ uint32_t red_empty(int b) const { return base + 8 * (2 * kMaxStages + kMaxBufs + b); }
+  __device__ uint32_t cl_full(int b) const { return base + 8 * (2 * kMaxStages + 2 * kMaxBufs + b); }
+  __device__ uint32_t cl_empty(int b) const { return base + 8 * (2 * kMaxStages + 3 * kMaxBufs + b); }
 };
-constexpr int kAbortFlagOffset = 1152;
-constexpr int kZeroAreaOffset = 1536;  // 32 zero bytes: x fragments of absent tokens
-constexpr int kBarRegionBytes = 2048;
-static_assert(8 * kWarps * kMaxWarpStages <= 1024, "barrier region");
+constexpr int kAbortFlagOffset = 8 * (2 * kMaxStages + 4 * kMaxBufs);
+constexpr int kZeroAreaOffset = kAbortFlagOffset + 32;  // 32 zero bytes: x of absent tokens
+constexpr int kBarRegionBytes = 1024;
+static_assert(kZeroAreaOffset + 32 <= kBarRegionBytes, "barrier region");
 
 struct Waiter {
   volatile int* abort;
@@ -93,10 +100,15 @@ struct Waiter {
   int* status;
 
   // Bounded wait for the completion of the phase with parity `par`.
-  template <bool kClusterScope>
+  // kPoll: probe without suspending (barriers completed by thread arrivals,
+  // where a suspended waiter may be woken late); otherwise try_wait (bulk-copy
+  // completion).
+  template <bool kClusterScope, bool kPoll = false>
   __device__ bool wait(uint32_t bar, uint32_t par) const {
     auto probe = [&]() {
-      return kClusterScope ? mbar_try_wait_cluster(bar, par) : mbar_try_wait(bar, par);
+      if constexpr (kClusterScope) return mbar_test_wait_cluster(bar, par);
+      else if constexpr (kPoll) return mbar_test_wait(bar, par);
+      else return mbar_try_wait(bar, par);
     };
     if (probe()) return true;
     const uint64_t t0 = global_ns();
@@ -111,9 +123,9 @@ struct Waiter {
     }
   }
   // Same, executed by a whole warp; the result is the same in every lane.
-  template <bool kClusterScope>
+  template <bool kClusterScope, bool kPoll = false>
   __device__ bool wait_warp(uint32_t bar, uint32_t par) const {
-    const bool ok = wait<kClusterScope>(bar, par);
+    const bool ok = wait<kClusterScope, kPoll>(bar, par);
     return __all_sync(0xffffffffu, ok) != 0;
   }
 };
@@ -139,35 +151,56 @@ __device__ __forceinline__ Work cta_work(const GemvArgs& a) {
   return w;
 }
 
-// The K slice of consumer warp `warp`: groups [gs, ge) of every job, cut into
-// nch chunks of up to chunk_groups groups.
+// The fixed K slice of consumer warp `warp` (x in registers): groups
+// [gs, ge) of every job.
 struct Slice {
-  int gs, ge, nch;
+  int gs, ge;
 };
-__device__ __forceinline__ Slice warp_slice(const Work& wk, int warp, int cg) {
+__device__ __forceinline__ Slice warp_slice(const Work& wk, int warp) {
   const int gc = wk.g_end - wk.g_begin;
   Slice s;
   s.gs = wk.g_begin + (warp * gc) / kWarps;
   s.ge = wk.g_begin + ((warp + 1) * gc) / kWarps;
-  s.nch = (s.ge - s.gs + cg - 1) / cg;
   return s;
 }
 
-// ------------------------------------------------------------------ chunk stream
-// Lane 0 of a consumer warp: bulk copies of chunk c of its slice into `slot`.
+// ------------------------------------------------------------------ producer
+// One thread: stage after stage, the codes and the scales of groups
+// [g0, g0 + ng) of one job, two bulk copies per stage.
 template <int BITS>
-__device__ __forceinline__ void issue_chunk(const GemvArgs& a, const Work& wk, const Slice& sl,
-                                            int c, uint32_t slot, uint32_t bar, uint64_t policy) {
+__device__ void producer(const GemvArgs& a, uint8_t* smem, const Bars& bars, const Waiter& wt,
+                         const Work& wk) {
   constexpr int kBlock = 128 * BITS;
-  const int j = c / sl.nch, ci = c - j * sl.nch;
-  const int g0 = sl.gs + ci * a.chunk_groups;
-  const int n = min(a.chunk_groups, sl.ge - g0);
-  const long long blk = (wk.rt_begin + j) * a.G + g0;
-  const uint32_t bc = static_cast<uint32_t>(n * kBlock);
-  const uint32_t bs = static_cast<uint32_t>(n * kScaleBytesPerBlock);
-  mbar_arrive_expect_tx(bar, bc + bs);
-  bulk_g2s(slot, a.codes + blk * kBlock, bc, bar, policy);
-  bulk_g2s(slot + a.chunk_groups * kBlock, a.scales + blk * 16, bs, bar, policy);
+  const uint64_t policy = l2_evict_first_policy();
+  const uint32_t ring = smem_addr(smem + a.off_ring);
+  const int sg = a.stage_groups;
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t issued = 0, last_par = 0;  // per-stage bookkeeping for the wind-down
+  bool ok = true;
+  for (int j = 0; j < wk.njobs && ok; ++j) {
+    const long long blk_job = (wk.rt_begin + j) * a.G;
+    for (int g0 = wk.g_begin; g0 < wk.g_end; g0 += sg) {
+      const int ng = min(sg, wk.g_end - g0);
+      if (!wt.wait<false>(bars.empty(stage), phase ^ 1)) { ok = false; break; }
+      const uint32_t bc = static_cast<uint32_t>(ng * kBlock);
+      const uint32_t bs = static_cast<uint32_t>(ng * kScaleBytesPerBlock);
+      const uint32_t dst = ring + stage * a.stage_bytes;
+      const long long blk = blk_job + g0;
+      mbar_arrive_expect_tx(bars.full(stage), bc + bs);
+      bulk_g2s(dst, a.codes + blk * kBlock, bc, bars.full(stage), policy);
+      bulk_g2s(dst + sg * kBlock, a.scales + blk * 16, bs, bars.full(stage), policy);
+      issued |= 1u << stage;
+      last_par = (last_par & ~(1u << stage)) | (phase << stage);
+      if (++stage == a.stages) { stage = 0; phase ^= 1; }
+    }
+  }
+  // Wind down: never leave the CTA with bulk copies in flight into its
+  // shared memory.  In normal operation every stage is already complete.
+  volatile int no_abort = 0;
+  const Waiter drain{&no_abort, wt.limit, wt.status};
+  for (int s = 0; s < a.stages; ++s)
+    if (issued & (1u << s)) (void)drain.wait<false>(bars.full(s), (last_par >> s) & 1u);
 }
 
 // ------------------------------------------------------------------ x tile
@@ -400,23 +433,49 @@ __device__ __forceinline__ void mma_group_xr(const uint8_t* blk, const uint8_t* 
   acc[3] = fmaf(s.y, d[3], acc[3]);
 }
 
-// Consumer warp of the register-resident-x variant (T <= 8): a chunk is the
-// warp's whole slice of one job (at most GWM groups), and the warp's x
-// fragments for that slice are loaded from global memory once per kernel.
+// ------------------------------------------------------------------ consumers
+// Hand a warp's 16 x T partial of job j to the epilogue (MMA accumulator
+// layout: lane q*4+r holds rows q, q+8 and tokens 8 nb + 2r, +1).
+// Buffer b = job % nbuf, nuse = job / nbuf (kept incrementally by the caller).
+template <int NT>
+__device__ __forceinline__ bool hand_partial_mma(const GemvArgs& a, uint8_t* smem,
+                                                 const Bars& bars, const Waiter& wt, int warp,
+                                                 int lane, int b, uint32_t nuse,
+                                                 const float (&acc)[NT][4]) {
+  const int q = lane >> 2, r = lane & 3;
+  const int T = a.T;
+  if (!wt.wait_warp<false, true>(bars.red_empty(b), (nuse & 1u) ^ 1u)) return false;
+  float* slot = reinterpret_cast<float*>(smem + a.off_red) + (b * kWarps + warp) * 16 * T;
+#pragma unroll
+  for (int nb = 0; nb < NT; ++nb) {
+    const int t0 = 8 * nb + 2 * r;
+    if (t0 < T) {
+      slot[t0 * 16 + q] = acc[nb][0];
+      slot[t0 * 16 + q + 8] = acc[nb][2];
+    }
+    if (t0 + 1 < T) {
+      slot[(t0 + 1) * 16 + q] = acc[nb][1];
+      slot[(t0 + 1) * 16 + q + 8] = acc[nb][3];
+    }
+  }
+  mbar_arrive(bars.red_full(b));  // every lane: count = 32 per warp
+  return true;
+}
+
+// x in registers (T <= 8): a stage holds the CTA's whole K range of one job;
+// the warp decodes its fixed slice of it.
 template <int BITS, int GWM>
 __device__ void consumer_xreg(const GemvArgs& a, uint8_t* smem, const Bars& bars,
-                              const Waiter& wt, const Work& wk, const Slice& sl, int warp,
-                              int lane, int issued) {
+                              const Waiter& wt, const Work& wk, int warp, int lane) {
   constexpr int kBlock = 128 * BITS;
   const int q = lane >> 2, r = lane & 3;
   const int T = a.T;
-  const int S = a.wstages;
-  const int n = sl.ge - sl.gs;  // groups of this warp's slice (<= GWM)
-  const uint32_t ring = smem_addr(smem + a.off_ring) + warp * S * a.wstage_bytes;
-  const uint8_t* ring_ptr = smem + a.off_ring + warp * S * a.wstage_bytes;
-  const uint8_t* scales_off = ring_ptr + a.chunk_groups * kBlock;
-  const uint64_t policy = l2_evict_first_policy();
-  float* red = reinterpret_cast<float*>(smem + a.off_red);
+  const Slice sl = warp_slice(wk, warp);
+  const int n = sl.ge - sl.gs;  // <= GWM
+  const int rel = sl.gs - wk.g_begin;
+  const uint8_t* ring = smem + a.off_ring;
+  const int codes_off = rel * kBlock;
+  const int scales_off = a.stage_groups * kBlock + rel * kScaleBytesPerBlock;
 
   uint32_t xr[GWM][8];
 #pragma unroll
@@ -436,68 +495,35 @@ __device__ void consumer_xreg(const GemvArgs& a, uint8_t* smem, const Bars& bars
 
   int stage = 0;
   uint32_t phase = 0;
-  int j = 0;
-  for (; j < wk.njobs; ++j) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (n > 0) {
-      if (!wt.wait_warp<false>(bars.full(warp, stage), phase)) break;
-      const uint8_t* slot = ring_ptr + stage * a.wstage_bytes;
-      const uint8_t* scb = scales_off + stage * a.wstage_bytes;
+  int rb = 0;        // partial buffer of this job
+  uint32_t rn = 0;   // uses of that buffer so far
+  for (int j = 0; j < wk.njobs; ++j) {
+    float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+    if (!wt.wait_warp<false>(bars.full(stage), phase)) return;
+    const uint8_t* st = ring + stage * a.stage_bytes;
 #pragma unroll
-      for (int i = 0; i < GWM; ++i)
-        if (i < n) mma_group_xr<BITS>(slot + i * kBlock, scb + i * kScaleBytesPerBlock, xr[i], lane, q, acc);
-      __syncwarp();
-      if (lane == 0 && j + S < wk.njobs) {
-        fence_proxy_async_smem();
-        issue_chunk<BITS>(a, wk, sl, j + S, ring + stage * a.wstage_bytes, bars.full(warp, stage),
-                          policy);
-        ++issued;
-      }
-      if (++stage == S) { stage = 0; phase ^= 1; }
-    }
-    const int b = j & 1;
-    const uint32_t nuse = static_cast<uint32_t>(j >> 1);
-    if (!wt.wait_warp<false>(bars.red_empty(b), (nuse & 1u) ^ 1u)) break;
-    float* slotp = red + (b * kWarps + warp) * 16 * T;
-    const int t0 = 2 * r;
-    if (t0 < T) {
-      slotp[t0 * 16 + q] = acc[0];
-      slotp[t0 * 16 + q + 8] = acc[2];
-    }
-    if (t0 + 1 < T) {
-      slotp[(t0 + 1) * 16 + q] = acc[1];
-      slotp[(t0 + 1) * 16 + q + 8] = acc[3];
-    }
-    mbar_arrive(bars.red_full(b));
-  }
-  // Wind down: drain chunks issued but not consumed (only after an error).
-  const int consumed = (n > 0) ? j : 0;
-  if (lane == 0 && issued > consumed) {
-    volatile int no_abort = 0;
-    const Waiter drain{&no_abort, wt.limit, wt.status};
-    for (int cc = consumed; cc < issued; ++cc)
-      (void)drain.wait<false>(bars.full(warp, cc % S), static_cast<uint32_t>((cc / S) & 1));
+    for (int i = 0; i < GWM; ++i)
+      if (i < n)
+        mma_group_xr<BITS>(st + codes_off + i * kBlock, st + scales_off + i * kScaleBytesPerBlock,
+                           xr[i], lane, q, acc[0]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars.empty(stage));
+    if (++stage == a.stages) { stage = 0; phase ^= 1; }
+    if (!hand_partial_mma<1>(a, smem, bars, wt, warp, lane, rb, rn, acc)) return;
+    if (++rb == a.nbuf) { rb = 0; ++rn; }
   }
 }
 
-// ------------------------------------------------------------------ consumer warps
-// Streams the warp's chunks, runs the per-group math and hands one 16 x T
-// partial per job to the epilogue.  Lane 0 issued chunks 0 .. wstages-1
-// before the call (see the kernel body).
+// x in shared memory: the warps take the groups of each stage in turn
+// (warp, warp + 16, ...).
 template <int BITS, int ROUTE, int NT>
-__device__ void consumer(const GemvArgs& a, uint8_t* smem, const Bars& bars, const Waiter& wt,
-                         const Work& wk, const Slice& sl, int warp, int lane, int issued) {
+__device__ void consumer_xsmem(const GemvArgs& a, uint8_t* smem, const Bars& bars,
+                               const Waiter& wt, const Work& wk, int warp, int lane) {
   constexpr int kBlock = 128 * BITS;
   const int q = lane >> 2, r = lane & 3;
   const int T = a.T;
-  const int cg = a.chunk_groups;
-  const int S = a.wstages;
-  const int total = wk.njobs * sl.nch;
-  const uint32_t ring = smem_addr(smem + a.off_ring) + warp * S * a.wstage_bytes;
-  const uint8_t* ring_ptr = smem + a.off_ring + warp * S * a.wstage_bytes;
-  const uint64_t policy = l2_evict_first_policy();
-  float* red = reinterpret_cast<float*>(smem + a.off_red);
-
+  const int sg = a.stage_groups;
+  const uint8_t* ring = smem + a.off_ring;
   // MMA route: x fragments of token 8 nb + q, or the zero area if absent.
   const uint8_t* xbase[NT];
   int xstep[NT];
@@ -511,10 +537,11 @@ __device__ void consumer(const GemvArgs& a, uint8_t* smem, const Bars& bars, con
   }
   const uint8_t* xf = smem + a.off_x + 64 * r;  // FMA route: entry (g, t, r) at (g T + t) 256 + 64 r
 
-  int c = 0, stage = 0;
+  int stage = 0;
   uint32_t phase = 0;
-  bool ok = true;
-  for (int j = 0; j < wk.njobs && ok; ++j) {
+  int rb = 0;        // partial buffer of this job
+  uint32_t rn = 0;   // uses of that buffer so far
+  for (int j = 0; j < wk.njobs; ++j) {
     float acc[NT][4];
     float facc[2][NT];
 #pragma unroll
@@ -522,50 +549,30 @@ __device__ void consumer(const GemvArgs& a, uint8_t* smem, const Bars& bars, con
       acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
       facc[0][nb] = facc[1][nb] = 0.f;
     }
-    for (int ci = 0; ci < sl.nch; ++ci, ++c) {
-      if (!wt.wait_warp<false>(bars.full(warp, stage), phase)) { ok = false; break; }
-      const uint8_t* slot = ring_ptr + stage * a.wstage_bytes;
-      const uint8_t* scb = slot + cg * kBlock;
-      const int g0 = sl.gs + ci * cg;
-      const int n = min(cg, sl.ge - g0);
+    for (int g0 = wk.g_begin; g0 < wk.g_end; g0 += sg) {
+      const int ng = min(sg, wk.g_end - g0);
+      if (!wt.wait_warp<false>(bars.full(stage), phase)) return;
+      const uint8_t* st = ring + stage * a.stage_bytes;
+      const uint8_t* scb = st + sg * kBlock;
       const int gx0 = g0 - wk.g_begin;
-      int i = 0;
-      if constexpr (ROUTE == kRouteMma) {
-        for (; i + 1 < n; i += 2) {
-          const uint8_t* xp0[NT];
-          const uint8_t* xp1[NT];
+      for (int gl = warp; gl < ng; gl += kWarps) {
+        if constexpr (ROUTE == kRouteMma) {
+          const uint8_t* xp[NT];
 #pragma unroll
-          for (int nb = 0; nb < NT; ++nb) {
-            xp0[nb] = xbase[nb] + (gx0 + i) * xstep[nb];
-            xp1[nb] = xbase[nb] + (gx0 + i + 1) * xstep[nb];
-          }
-          mma_group<BITS, NT>(slot + i * kBlock, scb + i * kScaleBytesPerBlock, xp0, lane, q, acc);
-          mma_group<BITS, NT>(slot + (i + 1) * kBlock, scb + (i + 1) * kScaleBytesPerBlock, xp1,
-                              lane, q, acc);
+          for (int nb = 0; nb < NT; ++nb) xp[nb] = xbase[nb] + (gx0 + gl) * xstep[nb];
+          mma_group<BITS, NT>(st + gl * kBlock, scb + gl * kScaleBytesPerBlock, xp, lane, q, acc);
+        } else {
+          ffma_group<BITS, NT>(st + gl * kBlock, scb + gl * kScaleBytesPerBlock,
+                               xf + (gx0 + gl) * T * 256, lane, q, T, facc);
         }
-        if (i < n) {
-          const uint8_t* xp0[NT];
-#pragma unroll
-          for (int nb = 0; nb < NT; ++nb) xp0[nb] = xbase[nb] + (gx0 + i) * xstep[nb];
-          mma_group<BITS, NT>(slot + i * kBlock, scb + i * kScaleBytesPerBlock, xp0, lane, q, acc);
-        }
-      } else {
-        for (; i < n; ++i)
-          ffma_group<BITS, NT>(slot + i * kBlock, scb + i * kScaleBytesPerBlock,
-                               xf + (gx0 + i) * T * 256, lane, q, T, facc);
       }
-      // Every lane has read the slot: refill it with the chunk S ahead.
       __syncwarp();
-      if (lane == 0 && c + S < total) {
-        fence_proxy_async_smem();
-        issue_chunk<BITS>(a, wk, sl, c + S, ring + stage * a.wstage_bytes, bars.full(warp, stage),
-                          policy);
-        ++issued;
-      }
-      if (++stage == S) { stage = 0; phase ^= 1; }
+      if (lane == 0) mbar_arrive(bars.empty(stage));
+      if (++stage == a.stages) { stage = 0; phase ^= 1; }
     }
-    if (!ok) break;
-    if constexpr (ROUTE == kRouteFfma) {
+    if constexpr (ROUTE == kRouteMma) {
+      if (!hand_partial_mma<NT>(a, smem, bars, wt, warp, lane, rb, rn, acc)) return;
+    } else {
       // Sum the four lanes of a row quad (fixed butterfly order).
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
@@ -577,106 +584,102 @@ __device__ void consumer(const GemvArgs& a, uint8_t* smem, const Bars& bars, con
           facc[h][t] = v;
         }
       }
-    }
-    // Hand the 16 x T partial of this warp to the epilogue warp.
-    const int b = j & 1;
-    const uint32_t nuse = static_cast<uint32_t>(j >> 1);
-    if (!wt.wait_warp<false>(bars.red_empty(b), (nuse & 1u) ^ 1u)) { ok = false; break; }
-    float* slotp = red + (b * kWarps + warp) * 16 * T;
-    if constexpr (ROUTE == kRouteMma) {
-#pragma unroll
-      for (int nb = 0; nb < NT; ++nb) {
-        const int t0 = 8 * nb + 2 * r;
-        if (t0 < T) {
-          slotp[t0 * 16 + q] = acc[nb][0];
-          slotp[t0 * 16 + q + 8] = acc[nb][2];
-        }
-        if (t0 + 1 < T) {
-          slotp[(t0 + 1) * 16 + q] = acc[nb][1];
-          slotp[(t0 + 1) * 16 + q + 8] = acc[nb][3];
-        }
-      }
-    } else {
+      if (!wt.wait_warp<false, true>(bars.red_empty(rb), (rn & 1u) ^ 1u)) return;
+      float* slot = reinterpret_cast<float*>(smem + a.off_red) + (rb * kWarps + warp) * 16 * T;
       if (r == 0) {
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           if (t < T) {
-            slotp[t * 16 + q] = facc[0][t];
-            slotp[t * 16 + q + 8] = facc[1][t];
+            slot[t * 16 + q] = facc[0][t];
+            slot[t * 16 + q + 8] = facc[1][t];
           }
         }
       }
+      mbar_arrive(bars.red_full(rb));
     }
-    mbar_arrive(bars.red_full(b));  // every lane: count = 32 per warp
-  }
-  // Wind down: never leave bulk copies in flight into this CTA's shared
-  // memory.  In normal operation every issued chunk has been consumed.
-  if (lane == 0 && issued > c) {
-    volatile int no_abort = 0;
-    const Waiter drain{&no_abort, wt.limit, wt.status};
-    for (int cc = c; cc < issued; ++cc)
-      (void)drain.wait<false>(bars.full(warp, cc % S), static_cast<uint32_t>((cc / S) & 1));
+    if (++rb == a.nbuf) { rb = 0; ++rn; }
   }
 }
 
 // ------------------------------------------------------------------ epilogue
-__device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& bars, const Waiter& wt,
-                         const Work& wk, int lane) {
+// Per job: sum the 16 warps' partials in warp order; with a K split, ranks
+// 1.. send their sums to rank 0 with asynchronous cluster stores whose bytes
+// complete rank 0's barrier, and rank 0 adds them in rank order and stores y.
+// No cluster-scope fence is needed: the peers' data is published by the
+// transaction count of st.async, and rank 0's "slot free" signal back to a
+// peer only orders rank 0's reads, which have completed once their values
+// have been added.  Lane l handles values l, l + 32, ... of the 16 x T tile;
+// `nvi` (uniform) of the MAXV register slots are in use, so nothing is issued
+// for tokens that do not exist.
+template <int MAXV>
+__device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& bars,
+                                const Waiter& wt, const Work& wk, int lane) {
   const int T = a.T;
   const int nv = 16 * T;             // values per row tile
+  const int nvi = (nv + 31) >> 5;    // value slots per lane in use (uniform)
   const int ks = a.ksplit;
   const float* red = reinterpret_cast<const float*>(smem + a.off_red);
   float* cl = reinterpret_cast<float*>(smem + a.off_cl);
+  const uint32_t cl_bytes = static_cast<uint32_t>((ks - 1) * nv * 4);
+  // Value lane + 32 i exists iff it is < nv; nv is a multiple of 16, so only
+  // the last slot in use can be partial.
+  auto has = [&](int i) { return i < nvi && lane + 32 * i < nv; };
+  int b = 0;
+  uint32_t n = 0;
   for (int j = 0; j < wk.njobs; ++j) {
-    const int b = j & 1;
-    const uint32_t n = static_cast<uint32_t>(j >> 1);
-    if (!wt.wait_warp<false>(bars.red_full(b), n & 1u)) return;
-    float v[8];
+    if (ks > 1 && wk.rank == 0 && lane == 0)
+      mbar_arrive_expect_tx_relaxed(bars.cl_full(b), cl_bytes);
+    if (!wt.wait_warp<false, true>(bars.red_full(b), n & 1u)) return;
+    float v[MAXV];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      float s = 0.f;
-      if (e < nv) {
-        const float* p = red + b * kWarps * nv + e;
+    for (int i = 0; i < MAXV; ++i) {
+      v[i] = 0.f;
+      if (has(i)) {
+        const float* p = red + b * kWarps * nv + lane + 32 * i;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) s += p[w * nv];
+        for (int w = 0; w < kWarps; ++w) v[i] += p[w * nv];
       }
-      v[i] = s;
     }
-    mbar_arrive(bars.red_empty(b));  // every lane: count 32
+    // Every lane has consumed its loads of the slot (the sums above); a
+    // release here would also wait for the previous job's y stores.
+    mbar_arrive_relaxed(bars.red_empty(b));  // every lane: count 32
+    bool store = true;
     if (ks > 1) {
       if (wk.rank != 0) {
-        if (!wt.wait_warp<true>(bars.cl_empty(b), (n & 1u) ^ 1u)) return;
+        if (!wt.wait_warp<false, true>(bars.cl_empty(b), (n & 1u) ^ 1u)) return;
         const uint32_t dst0 =
-            map_to_rank(smem_addr(cl + (b * (ks - 1) + (wk.rank - 1)) * nv), 0);
+            map_to_rank(smem_addr(cl + (b * (ks - 1) + (wk.rank - 1)) * nv + lane), 0);
+        const uint32_t bar0 = map_to_rank(bars.cl_full(b), 0);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int e = lane + 32 * i;
-          if (e < nv) st_cluster_f32(dst0 + 4 * e, v[i]);
+        for (int i = 0; i < MAXV; ++i)
+          if (has(i)) st_async_f32(dst0 + 128 * i, v[i], bar0);
+        store = false;
+      } else {
+        if (!wt.wait_warp<false, true>(bars.cl_full(b), n & 1u)) return;
+        for (int p = 1; p < ks; ++p) {
+          const float* src = cl + (b * (ks - 1) + (p - 1)) * nv + lane;
+#pragma unroll
+          for (int i = 0; i < MAXV; ++i)
+            if (has(i)) v[i] += src[32 * i];
         }
-        mbar_arrive_remote(map_to_rank(bars.cl_full(b), 0));
-        continue;
-      }
-      if (!wt.wait_warp<true>(bars.cl_full(b), n & 1u)) return;
-      for (int p = 1; p < ks; ++p) {
-        const float* src = cl + (b * (ks - 1) + (p - 1)) * nv;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int e = lane + 32 * i;
-          if (e < nv) v[i] += src[e];
+        __syncwarp();
+        if (lane == 0) {
+          for (int p = 1; p < ks; ++p) mbar_arrive_remote_relaxed(map_to_rank(bars.cl_empty(b), p));
         }
-      }
-      for (int p = 1; p < ks; ++p) mbar_arrive_remote(map_to_rank(bars.cl_empty(b), p));
-    }
-    const long long row0 = (wk.rt_begin + j) * 16;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      if (e < nv) {
-        const int tok = e >> 4, row = e & 15;
-        if (row0 + row < a.N) a.y[static_cast<long long>(tok) * a.N + row0 + row] = v[i];
       }
     }
+    if (store) {
+      const long long row0 = (wk.rt_begin + j) * 16;
+#pragma unroll
+      for (int i = 0; i < MAXV; ++i) {
+        const int e = lane + 32 * i;
+        if (has(i)) {
+          const int tok = e >> 4, row = e & 15;
+          if (row0 + row < a.N) a.y[static_cast<long long>(tok) * a.N + row0 + row] = v[i];
+        }
+      }
+    }
+    if (++b == a.nbuf) { b = 0; ++n; }
   }
 }
 
@@ -691,13 +694,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   const Work wk = cta_work(a);
 
   if (threadIdx.x == 0) {
-    for (int w = 0; w < kWarps; ++w)
-      for (int s = 0; s < a.wstages; ++s) mbar_init(bars.full(w, s), 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(bars.full(s), 1);
+      mbar_init(bars.empty(s), kWarps);
+    }
+    for (int b = 0; b < a.nbuf; ++b) {
       mbar_init(bars.red_full(b), 32 * kWarps);
       mbar_init(bars.red_empty(b), 32);
-      mbar_init(bars.cl_full(b), 32 * (a.ksplit > 1 ? a.ksplit - 1 : 1));
-      mbar_init(bars.cl_empty(b), 32);
+      mbar_init(bars.cl_full(b), 1);   // rank 0's expect_tx; peers' bytes
+      mbar_init(bars.cl_empty(b), 1);  // rank 0, once per job
     }
     *abort_flag = 0;
     for (int i = 0; i < 8; ++i) reinterpret_cast<uint32_t*>(smem + kZeroAreaOffset)[i] = 0u;
@@ -709,22 +714,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   griddep_launch_dependents();
   if (a.ksplit > 1) cluster_sync_all(); else __syncthreads();
 
-  if (warp < kWarps) {
-    const Slice sl = warp_slice(wk, warp, a.chunk_groups);
-    int issued = 0;
-    // Packed weights are read-only for the whole stream, so the first chunks
-    // may be requested before the previous kernel has finished.
-    if (lane == 0) {
-      const int total = wk.njobs * sl.nch;
-      const uint64_t policy = l2_evict_first_policy();
-      const uint32_t ring = smem_addr(smem + a.off_ring) + warp * a.wstages * a.wstage_bytes;
-      for (; issued < a.wstages && issued < total; ++issued)
-        issue_chunk<BITS>(a, wk, sl, issued, ring + issued * a.wstage_bytes,
-                          bars.full(warp, issued), policy);
+  if (warp == kProducerWarp) {
+    // Packed weights are read-only for the whole stream, so streaming them
+    // may overlap the tail of the previous kernel.
+    if (lane == 0) producer<BITS>(a, smem, bars, wt, wk);
+  } else if (warp == kEpilogueWarp) {
+    griddep_wait();
+    // Value slots per lane: 16 x T values over 32 lanes.
+    if constexpr (ROUTE == kRouteMma && NTOK == 2) {
+      epilogue<8>(a, smem, bars, wt, wk, lane);
+    } else {
+      epilogue<4>(a, smem, bars, wt, wk, lane);
     }
+  } else {
     griddep_wait();
     if constexpr (ROUTE == kRouteMma && NTOK == kNtokXreg) {
-      consumer_xreg<BITS, kXregMaxGroups>(a, smem, bars, wt, wk, sl, warp, lane, issued);
+      consumer_xreg<BITS, kXregMaxGroups>(a, smem, bars, wt, wk, warp, lane);
     } else {
       if constexpr (ROUTE == kRouteMma) {
         stage_x_bf16(a, smem, wk, threadIdx.x, kWarps * 32);
@@ -732,11 +737,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         stage_x_f32(a, smem, wk, threadIdx.x, kWarps * 32);
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
-      consumer<BITS, ROUTE, NTOK>(a, smem, bars, wt, wk, sl, warp, lane, issued);
+      consumer_xsmem<BITS, ROUTE, NTOK>(a, smem, bars, wt, wk, warp, lane);
     }
-  } else {
-    griddep_wait();
-    epilogue(a, smem, bars, wt, wk, lane);
   }
   // No CTA may leave while cluster peers can still write into its shared
   // memory or arrive on its barriers.

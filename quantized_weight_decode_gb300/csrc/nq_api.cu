@@ -113,26 +113,29 @@ const void* kernel_for(int bits, int route, int ntok) {
 int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
 struct Plan {
-  int route = 0, ntok = 0, ks = 1, clusters = 0, cg = 1, stages = 0, stage_bytes = 0;
+  int route = 0, ntok = 0, ks = 1, clusters = 0, sg = 1, stages = 0, stage_bytes = 0, nbuf = 2;
   int smem = 0, off_ring = 0, off_red = 0, off_cl = 0, off_x = 0;
   const void* func = nullptr;
   double est_us = 0;
 };
 
-// Shared-memory layout for a K-split and a chunk size; false if it does not
-// fit with at least `min_stages` ring slots per consumer warp.
-bool layout_for(const Plan& base, int G, int T, int bits, int ks, int cg, int min_stages,
+// Shared-memory layout for a K-split and a stage size (64-groups per stage);
+// false if fewer than `min_stages` stages fit.
+bool layout_for(const Plan& base, int G, int T, int bits, int ks, int sg, int min_stages,
                 int smem_optin, Plan* out) {
   Plan p = base;
   p.ks = ks;
-  p.cg = cg;
+  p.sg = sg;
   const int gc_max = (G + ks - 1) / ks;
   const bool x_in_regs = p.route == NQ_ROUTE_MMA && p.ntok == kNtokXreg;
   const long long x_bytes =
       x_in_regs ? 0 : 1LL * gc_max * T * (p.route == NQ_ROUTE_MMA ? 128 : 256);
-  const int red_bytes = 2 * kWarps * 16 * T * 4;
-  const int cl_bytes = ks > 1 ? 2 * (ks - 1) * 16 * T * 4 : 0;
-  p.stage_bytes = align_up(cg * (block_bytes(bits) + kScaleBytesPerBlock), 128);
+  // Partial-sum buffers in flight between the warps, the epilogue and the
+  // cluster's rank 0: deep for small T (cheap), shallow for large T.
+  p.nbuf = T <= 2 ? kMaxBufs : T <= 4 ? 6 : T <= 8 ? 4 : 2;
+  const int red_bytes = p.nbuf * kWarps * 16 * T * 4;
+  const int cl_bytes = ks > 1 ? p.nbuf * (ks - 1) * 16 * T * 4 : 0;
+  p.stage_bytes = align_up(sg * (block_bytes(bits) + kScaleBytesPerBlock), 128);
   p.off_red = kBarRegionBytes;
   p.off_cl = p.off_red + align_up(red_bytes, 128);
   p.off_x = p.off_cl + align_up(cl_bytes, 128);
@@ -140,10 +143,9 @@ bool layout_for(const Plan& base, int G, int T, int bits, int ks, int cg, int mi
       p.off_x + align_up(static_cast<int>(std::min<long long>(x_bytes, 1 << 30)), 128);
   if (fixed >= smem_optin) return false;
   p.off_ring = static_cast<int>(fixed);
-  const long long per_warp = (smem_optin - fixed) / kWarps;
-  p.stages = static_cast<int>(std::min<long long>(kMaxWarpStages, per_warp / p.stage_bytes));
+  p.stages = static_cast<int>(std::min<long long>(kMaxStages, (smem_optin - fixed) / p.stage_bytes));
   if (p.stages < min_stages) return false;
-  p.smem = p.off_ring + kWarps * p.stages * p.stage_bytes;
+  p.smem = p.off_ring + p.stages * p.stage_bytes;
   *out = p;
   return true;
 }
@@ -199,12 +201,14 @@ int max_clusters(int dev, const DevInfo& d, const void* func, int ks, int smem) 
 // Rough time model: the weight stream at the HBM rate while every SM is busy,
 // the last partial wave at the per-SM rate of the SMs that still have work.
 // The per-SM rate is capped by the bytes a CTA keeps in flight (Little's law
-// with ~1 us of memory latency).
+// with ~1 us of memory latency) and by the bulk-copy requests it issues
+// (~60 ns each, two per stage).
 double estimate_us(const Plan& p, long long Nt, int G, int bits) {
-  const double bw = 6.5e12, bw_sm_max = 1.1e11, latency_s = 1.0e-6;
+  const double bw = 6.5e12, bw_sm_max = 1.1e11, latency_s = 1.0e-6, request_s = 60e-9;
   const double group_bytes = block_bytes(bits) + kScaleBytesPerBlock;
-  const double inflight = static_cast<double>(kWarps) * p.stages * p.cg * group_bytes;
-  const double bw_sm = std::min(bw_sm_max, inflight / latency_s);
+  const double inflight = static_cast<double>(p.stages) * p.sg * group_bytes;
+  const double stage_rate = p.sg * group_bytes / (2 * request_s);
+  const double bw_sm = std::min(std::min(bw_sm_max, inflight / latency_s), stage_rate);
   const int gc_max = (G + p.ks - 1) / p.ks;
   const double job_bytes = gc_max * group_bytes;
   const long long C = p.clusters;
@@ -255,19 +259,22 @@ int make_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, Plan
   for (int ks : cands) {
     if (ksplit != 0 && ks != ksplit) continue;
     if (ks > G) continue;
-    const int gw_max = ((G + ks - 1) / ks + kWarps - 1) / kWarps;
+    const int gc_max = (G + ks - 1) / ks;
+    const int gw_max = (gc_max + kWarps - 1) / kWarps;
     Plan p;
     bool fit = false;
     if (route == NQ_ROUTE_MMA && T <= 8 && gw_max <= kXregMaxGroups) {
-      // x held in registers; a chunk is a warp's whole slice of one job.
-      fit = layout_for(xreg, G, T, bits, ks, gw_max, 2, d->smem_optin, &p);
+      // x held in registers; a stage is the CTA's whole K range of one job.
+      fit = layout_for(xreg, G, T, bits, ks, gc_max, 2, d->smem_optin, &p);
     }
-    // Otherwise x in shared memory; chunk size: as many groups of a warp's
-    // slice as fit with 3 ring slots per warp, else fewer groups, else 2
-    // slots of one group.
-    for (int cg = std::min(gw_max, kMaxChunkGroups); cg >= 1 && !fit; --cg)
-      fit = layout_for(base, G, T, bits, ks, cg, 3, d->smem_optin, &p);
-    if (!fit) fit = layout_for(base, G, T, bits, ks, 1, 2, d->smem_optin, &p);
+    // Otherwise x in shared memory; a stage is the job's K range cut into
+    // `parts` equal pieces, the fewest that leave at least 3 stages (2 when
+    // a piece is down to one group per warp).
+    for (int parts = 1; !fit && parts <= gc_max; ++parts) {
+      const int sg = (gc_max + parts - 1) / parts;
+      fit = layout_for(base, G, T, bits, ks, sg, sg <= kWarps ? 2 : 3, d->smem_optin, &p);
+      if (sg <= kWarps) break;
+    }
     if (!fit) continue;
     const int mc = max_clusters(dev, *d, p.func, ks, p.smem);
     if (mc <= 0) continue;
@@ -299,13 +306,14 @@ int launch_plan(const Plan& p, const void* packed, const uint16_t* scales, const
   a.Nt = static_cast<int>((N + kTileRows - 1) / kTileRows);
   a.ksplit = p.ks;
   a.clusters = p.clusters;
-  a.chunk_groups = p.cg;
-  a.wstages = p.stages;
-  a.wstage_bytes = p.stage_bytes;
+  a.stage_groups = p.sg;
+  a.stages = p.stages;
+  a.stage_bytes = p.stage_bytes;
   a.off_ring = p.off_ring;
   a.off_red = p.off_red;
   a.off_cl = p.off_cl;
   a.off_x = p.off_x;
+  a.nbuf = p.nbuf;
   a.wait_ns = static_cast<unsigned long long>(std::max(1, env_int("NQ_WAIT_MS", 2000))) * 1000000ULL;
   a.status = d->status;
 
