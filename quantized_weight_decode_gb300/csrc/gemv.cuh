@@ -19,10 +19,11 @@
 //                          tile when it fits -- with two 1-D bulk copies per
 //                          stage (codes, scales; TMA engine, L2 evict-first)
 //                          into a ring of shared-memory stages;
-//   warp 17    epilogue  : sums the 16 per-warp partials of a row tile in a
-//                          fixed order, adds the partials of the other CTAs of
-//                          its cluster (K split, asynchronous distributed
-//                          shared-memory stores, rank order) and stores y.
+//   warp 17,18 epilogue  : taking jobs in turn, sum the 16 per-warp partials
+//                          of a row tile in a fixed order, add the partials of
+//                          the other CTAs of the cluster (K split,
+//                          asynchronous distributed shared-memory stores, rank
+//                          order) and store y.
 //
 // Few large copies matter: the bulk-copy engine of an SM serves a limited
 // number of requests per microsecond, so small per-warp copies cap the
@@ -48,8 +49,9 @@ namespace nq {
 
 constexpr int kWarps = 16;                   // consumer warps
 constexpr int kProducerWarp = kWarps;
-constexpr int kEpilogueWarp = kWarps + 1;
-constexpr int kThreads = (kWarps + 2) * 32;
+constexpr int kEpilogueWarp = kWarps + 1;     // first of kEpiWarps epilogue warps
+constexpr int kEpiWarps = 2;                  // epilogue warps, taking jobs in turn
+constexpr int kThreads = (kWarps + 1 + kEpiWarps) * 32;
 constexpr int kMaxStages = 16;               // stages of the shared-memory ring
 constexpr int kMaxBufs = 8;                  // partial-sum buffers (warps -> epilogue, peers -> rank 0)
 constexpr int kStatusTimeout = -5;
@@ -58,6 +60,10 @@ constexpr int kStatusTimeout = -5;
 // most kXregMaxGroups groups per warp slice), FMA route: NTOK = max tokens.
 constexpr int kNtokXreg = 3;
 constexpr int kXregMaxGroups = 6;
+// kNtokXreg2: two token blocks (T <= 16), x in registers, at most
+// kXreg2MaxGroups groups per warp slice.
+constexpr int kNtokXreg2 = 4;
+constexpr int kXreg2MaxGroups = 3;
 
 enum Route : int { kRouteMma = 1, kRouteFfma = 2 };
 
@@ -404,33 +410,39 @@ __device__ __forceinline__ void ffma_group(const uint8_t* blk, const uint8_t* sc
   }
 }
 
-// Same as mma_group for one token block, with the lane's x fragments of the
-// group held in registers: xr[2 js] / xr[2 js + 1] are B fragments b0 / b1 of
-// K slice js.
-template <int BITS>
+// Same as mma_group with the lane's x fragments of the group held in
+// registers: xr[nb][2 js] / xr[nb][2 js + 1] are B fragments b0 / b1 of K
+// slice js for token block nb.
+template <int BITS, int NT>
 __device__ __forceinline__ void mma_group_xr(const uint8_t* blk, const uint8_t* sc,
-                                             const uint32_t (&xr)[8], int lane, int q,
-                                             float (&acc)[4]) {
+                                             const uint32_t (&xr)[NT][8], int lane, int q,
+                                             float (&acc)[NT][4]) {
   uint32_t w[BITS];
   load_lane_words<BITS>(blk, lane, w);
   const float2 s = __half22float2(*reinterpret_cast<const __half2*>(sc + 4 * q));
-  float d[4];
+  float d[NT][4];
 #pragma unroll
   for (int js = 0; js < 4; ++js) {
     const uint32_t a0 = pair_codes_bf16<BITS>(w, 4 * js + 0);
     const uint32_t a1 = pair_codes_bf16<BITS>(w, 4 * js + 1);
     const uint32_t a2 = pair_codes_bf16<BITS>(w, 4 * js + 2);
     const uint32_t a3 = pair_codes_bf16<BITS>(w, 4 * js + 3);
-    if (js == 0) {
-      mma_16816_zc(d, a0, a1, a2, a3, xr[0], xr[1]);
-    } else {
-      mma_16816(d, a0, a1, a2, a3, xr[2 * js], xr[2 * js + 1]);
+#pragma unroll
+    for (int nb = 0; nb < NT; ++nb) {
+      if (js == 0) {
+        mma_16816_zc(d[nb], a0, a1, a2, a3, xr[nb][0], xr[nb][1]);
+      } else {
+        mma_16816(d[nb], a0, a1, a2, a3, xr[nb][2 * js], xr[nb][2 * js + 1]);
+      }
     }
   }
-  acc[0] = fmaf(s.x, d[0], acc[0]);
-  acc[1] = fmaf(s.x, d[1], acc[1]);
-  acc[2] = fmaf(s.y, d[2], acc[2]);
-  acc[3] = fmaf(s.y, d[3], acc[3]);
+#pragma unroll
+  for (int nb = 0; nb < NT; ++nb) {
+    acc[nb][0] = fmaf(s.x, d[nb][0], acc[nb][0]);
+    acc[nb][1] = fmaf(s.x, d[nb][1], acc[nb][1]);
+    acc[nb][2] = fmaf(s.y, d[nb][2], acc[nb][2]);
+    acc[nb][3] = fmaf(s.y, d[nb][3], acc[nb][3]);
+  }
 }
 
 // ------------------------------------------------------------------ consumers
@@ -444,7 +456,7 @@ __device__ __forceinline__ bool hand_partial_mma(const GemvArgs& a, uint8_t* sme
                                                  const float (&acc)[NT][4]) {
   const int q = lane >> 2, r = lane & 3;
   const int T = a.T;
-  if (!wt.wait_warp<false, true>(bars.red_empty(b), (nuse & 1u) ^ 1u)) return false;
+  if (!wt.wait_warp<false>(bars.red_empty(b), (nuse & 1u) ^ 1u)) return false;
   float* slot = reinterpret_cast<float*>(smem + a.off_red) + (b * kWarps + warp) * 16 * T;
 #pragma unroll
   for (int nb = 0; nb < NT; ++nb) {
@@ -462,9 +474,10 @@ __device__ __forceinline__ bool hand_partial_mma(const GemvArgs& a, uint8_t* sme
   return true;
 }
 
-// x in registers (T <= 8): a stage holds the CTA's whole K range of one job;
-// the warp decodes its fixed slice of it.
-template <int BITS, int GWM>
+// x in registers: a stage holds the CTA's whole K range of one job; the warp
+// decodes its fixed slice of it (at most GWM groups) against x fragments of
+// NT token blocks loaded once per kernel.
+template <int BITS, int GWM, int NT>
 __device__ void consumer_xreg(const GemvArgs& a, uint8_t* smem, const Bars& bars,
                               const Waiter& wt, const Work& wk, int warp, int lane) {
   constexpr int kBlock = 128 * BITS;
@@ -477,18 +490,22 @@ __device__ void consumer_xreg(const GemvArgs& a, uint8_t* smem, const Bars& bars
   const int codes_off = rel * kBlock;
   const int scales_off = a.stage_groups * kBlock + rel * kScaleBytesPerBlock;
 
-  uint32_t xr[GWM][8];
+  uint32_t xr[GWM][NT][8];
 #pragma unroll
   for (int i = 0; i < GWM; ++i) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) xr[i][e] = 0u;
-    if (i < n && q < T) {
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(
-          a.x + static_cast<long long>(q) * a.K + 64LL * (sl.gs + i) + 2 * r);
+    for (int nb = 0; nb < NT; ++nb) {
 #pragma unroll
-      for (int js = 0; js < 4; ++js) {
-        xr[i][2 * js] = __ldg(src + 8 * js);
-        xr[i][2 * js + 1] = __ldg(src + 8 * js + 4);
+      for (int e = 0; e < 8; ++e) xr[i][nb][e] = 0u;
+      const int tok = 8 * nb + q;
+      if (i < n && tok < T) {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(
+            a.x + static_cast<long long>(tok) * a.K + 64LL * (sl.gs + i) + 2 * r);
+#pragma unroll
+        for (int js = 0; js < 4; ++js) {
+          xr[i][nb][2 * js] = __ldg(src + 8 * js);
+          xr[i][nb][2 * js + 1] = __ldg(src + 8 * js + 4);
+        }
       }
     }
   }
@@ -498,18 +515,20 @@ __device__ void consumer_xreg(const GemvArgs& a, uint8_t* smem, const Bars& bars
   int rb = 0;        // partial buffer of this job
   uint32_t rn = 0;   // uses of that buffer so far
   for (int j = 0; j < wk.njobs; ++j) {
-    float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+    float acc[NT][4];
+#pragma unroll
+    for (int nb = 0; nb < NT; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
     if (!wt.wait_warp<false>(bars.full(stage), phase)) return;
     const uint8_t* st = ring + stage * a.stage_bytes;
 #pragma unroll
     for (int i = 0; i < GWM; ++i)
       if (i < n)
-        mma_group_xr<BITS>(st + codes_off + i * kBlock, st + scales_off + i * kScaleBytesPerBlock,
-                           xr[i], lane, q, acc[0]);
+        mma_group_xr<BITS, NT>(st + codes_off + i * kBlock,
+                               st + scales_off + i * kScaleBytesPerBlock, xr[i], lane, q, acc);
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.empty(stage));
     if (++stage == a.stages) { stage = 0; phase ^= 1; }
-    if (!hand_partial_mma<1>(a, smem, bars, wt, warp, lane, rb, rn, acc)) return;
+    if (!hand_partial_mma<NT>(a, smem, bars, wt, warp, lane, rb, rn, acc)) return;
     if (++rb == a.nbuf) { rb = 0; ++rn; }
   }
 }
@@ -584,7 +603,7 @@ __device__ void consumer_xsmem(const GemvArgs& a, uint8_t* smem, const Bars& bar
           facc[h][t] = v;
         }
       }
-      if (!wt.wait_warp<false, true>(bars.red_empty(rb), (rn & 1u) ^ 1u)) return;
+      if (!wt.wait_warp<false>(bars.red_empty(rb), (rn & 1u) ^ 1u)) return;
       float* slot = reinterpret_cast<float*>(smem + a.off_red) + (rb * kWarps + warp) * 16 * T;
       if (r == 0) {
 #pragma unroll
@@ -611,9 +630,11 @@ __device__ void consumer_xsmem(const GemvArgs& a, uint8_t* smem, const Bars& bar
 // have been added.  Lane l handles values l, l + 32, ... of the 16 x T tile;
 // `nvi` (uniform) of the MAXV register slots are in use, so nothing is issued
 // for tokens that do not exist.
+// Epilogue warp `ew` handles jobs ew, ew + kEpiWarps, ...; nbuf is a multiple
+// of kEpiWarps, so each partial buffer always belongs to the same warp.
 template <int MAXV>
 __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& bars,
-                                const Waiter& wt, const Work& wk, int lane) {
+                                const Waiter& wt, const Work& wk, int ew, int lane) {
   const int T = a.T;
   const int nv = 16 * T;             // values per row tile
   const int nvi = (nv + 31) >> 5;    // value slots per lane in use (uniform)
@@ -624,12 +645,12 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
   // Value lane + 32 i exists iff it is < nv; nv is a multiple of 16, so only
   // the last slot in use can be partial.
   auto has = [&](int i) { return i < nvi && lane + 32 * i < nv; };
-  int b = 0;
-  uint32_t n = 0;
-  for (int j = 0; j < wk.njobs; ++j) {
+  int b = ew;        // buffer of job j (j % nbuf)
+  uint32_t n = 0;    // uses of that buffer so far (j / nbuf)
+  for (int j = ew; j < wk.njobs; j += kEpiWarps) {
     if (ks > 1 && wk.rank == 0 && lane == 0)
       mbar_arrive_expect_tx_relaxed(bars.cl_full(b), cl_bytes);
-    if (!wt.wait_warp<false, true>(bars.red_full(b), n & 1u)) return;
+    if (!wt.wait_warp<false>(bars.red_full(b), n & 1u)) return;
     float v[MAXV];
 #pragma unroll
     for (int i = 0; i < MAXV; ++i) {
@@ -646,7 +667,7 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
     bool store = true;
     if (ks > 1) {
       if (wk.rank != 0) {
-        if (!wt.wait_warp<false, true>(bars.cl_empty(b), (n & 1u) ^ 1u)) return;
+        if (!wt.wait_warp<false>(bars.cl_empty(b), (n & 1u) ^ 1u)) return;
         const uint32_t dst0 =
             map_to_rank(smem_addr(cl + (b * (ks - 1) + (wk.rank - 1)) * nv + lane), 0);
         const uint32_t bar0 = map_to_rank(bars.cl_full(b), 0);
@@ -655,7 +676,7 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
           if (has(i)) st_async_f32(dst0 + 128 * i, v[i], bar0);
         store = false;
       } else {
-        if (!wt.wait_warp<false, true>(bars.cl_full(b), n & 1u)) return;
+        if (!wt.wait_warp<false>(bars.cl_full(b), n & 1u)) return;
         for (int p = 1; p < ks; ++p) {
           const float* src = cl + (b * (ks - 1) + (p - 1)) * nv + lane;
 #pragma unroll
@@ -679,7 +700,8 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
         }
       }
     }
-    if (++b == a.nbuf) { b = 0; ++n; }
+    b += kEpiWarps;
+    if (b >= a.nbuf) { b -= a.nbuf; ++n; }
   }
 }
 
@@ -718,18 +740,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     // Packed weights are read-only for the whole stream, so streaming them
     // may overlap the tail of the previous kernel.
     if (lane == 0) producer<BITS>(a, smem, bars, wt, wk);
-  } else if (warp == kEpilogueWarp) {
+  } else if (warp >= kEpilogueWarp) {
+    const int ew = warp - kEpilogueWarp;
     griddep_wait();
     // Value slots per lane: 16 x T values over 32 lanes.
-    if constexpr (ROUTE == kRouteMma && NTOK == 2) {
-      epilogue<8>(a, smem, bars, wt, wk, lane);
+    if constexpr (ROUTE == kRouteMma && (NTOK == 2 || NTOK == kNtokXreg2)) {
+      epilogue<8>(a, smem, bars, wt, wk, ew, lane);
     } else {
-      epilogue<4>(a, smem, bars, wt, wk, lane);
+      epilogue<4>(a, smem, bars, wt, wk, ew, lane);
     }
   } else {
     griddep_wait();
     if constexpr (ROUTE == kRouteMma && NTOK == kNtokXreg) {
-      consumer_xreg<BITS, kXregMaxGroups>(a, smem, bars, wt, wk, warp, lane);
+      consumer_xreg<BITS, kXregMaxGroups, 1>(a, smem, bars, wt, wk, warp, lane);
+    } else if constexpr (ROUTE == kRouteMma && NTOK == kNtokXreg2) {
+      consumer_xreg<BITS, kXreg2MaxGroups, 2>(a, smem, bars, wt, wk, warp, lane);
     } else {
       if constexpr (ROUTE == kRouteMma) {
         stage_x_bf16(a, smem, wk, threadIdx.x, kWarps * 32);

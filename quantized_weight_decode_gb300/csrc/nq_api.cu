@@ -127,12 +127,16 @@ bool layout_for(const Plan& base, int G, int T, int bits, int ks, int sg, int mi
   p.ks = ks;
   p.sg = sg;
   const int gc_max = (G + ks - 1) / ks;
-  const bool x_in_regs = p.route == NQ_ROUTE_MMA && p.ntok == kNtokXreg;
+  const bool x_in_regs = p.route == NQ_ROUTE_MMA && (p.ntok == kNtokXreg || p.ntok == kNtokXreg2);
   const long long x_bytes =
       x_in_regs ? 0 : 1LL * gc_max * T * (p.route == NQ_ROUTE_MMA ? 128 : 256);
   // Partial-sum buffers in flight between the warps, the epilogue and the
   // cluster's rank 0: deep for small T (cheap), shallow for large T.
+  // (a multiple of kEpiWarps: each buffer belongs to one epilogue warp)
   p.nbuf = T <= 2 ? kMaxBufs : T <= 4 ? 6 : T <= 8 ? 4 : 2;
+  static_assert(kMaxBufs % kEpiWarps == 0 && 6 % kEpiWarps == 0 && 4 % kEpiWarps == 0 &&
+                    2 % kEpiWarps == 0,
+                "buffer counts must be multiples of the epilogue warps");
   const int red_bytes = p.nbuf * kWarps * 16 * T * 4;
   const int cl_bytes = ks > 1 ? p.nbuf * (ks - 1) * 16 * T * 4 : 0;
   p.stage_bytes = align_up(sg * (block_bytes(bits) + kScaleBytesPerBlock), 128);
@@ -244,10 +248,13 @@ int make_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, Plan
   base.ntok = route == NQ_ROUTE_MMA ? (T <= 8 ? 1 : 2) : kFfmaMaxT;
   base.func = kernel_for(bits, route, base.ntok);
   if (int rc = prepare_func(dev, base.func, d->smem_optin)) return rc;
+  // x-in-register variant: one token block (T <= 8, slices of up to
+  // kXregMaxGroups groups) or two (T <= 16, up to kXreg2MaxGroups).
   Plan xreg = base;
-  xreg.ntok = kNtokXreg;
-  xreg.func = kernel_for(bits, route, kNtokXreg);
-  if (route == NQ_ROUTE_MMA && T <= 8) {
+  xreg.ntok = T <= 8 ? kNtokXreg : kNtokXreg2;
+  xreg.func = kernel_for(bits, route, xreg.ntok);
+  const int xreg_max_groups = T <= 8 ? kXregMaxGroups : kXreg2MaxGroups;
+  if (route == NQ_ROUTE_MMA) {
     if (int rc = prepare_func(dev, xreg.func, d->smem_optin)) return rc;
   }
 
@@ -263,7 +270,7 @@ int make_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, Plan
     const int gw_max = (gc_max + kWarps - 1) / kWarps;
     Plan p;
     bool fit = false;
-    if (route == NQ_ROUTE_MMA && T <= 8 && gw_max <= kXregMaxGroups) {
+    if (route == NQ_ROUTE_MMA && gw_max <= xreg_max_groups) {
       // x held in registers; a stage is the CTA's whole K range of one job.
       fit = layout_for(xreg, G, T, bits, ks, gc_max, 2, d->smem_optin, &p);
     }
