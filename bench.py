@@ -420,6 +420,62 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ single shape
+CONFIG_SHAPES = {
+    "tiny_q4": (512, 256, 4, (1,)),
+    "gate_up_q4": (HIDDEN, 2 * INTER, 4, (1,)),
+    "down_q5": (INTER, HIDDEN, 5, (1, 8)),
+    "head_q6": (HIDDEN, VOCAB, 6, (1, 2, 4, 8)),
+}
+
+
+def run_single(spec: str, reps: int, seed: int):
+    """Time one GEMV shape "K,N,bits,T" (or a config name above, every T):
+    `reps` launches over enough distinct packed copies (>= 3x L2) that no
+    launch finds its weights in L2.  Prints one JSON line per (shape, T)."""
+    import torch
+
+    import quantized_weight_decode_gb300 as nqp
+    torch.cuda.set_device(0)
+    nqp.build()
+    if spec in CONFIG_SHAPES:
+        K, N, bits, Ts = CONFIG_SHAPES[spec]
+    else:
+        K, N, bits, T = (int(v) for v in spec.split(","))
+        Ts = (T,)
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    w = torch.randn((N, K), generator=g, device=dev, dtype=torch.float32).mul_(0.02)
+    qw = nqp.QuantizedWeight.from_fp32(w, bits)
+    del w
+    nbytes = packed_bytes(bits, K, N)
+    copies = [qw] + [nqp.QuantizedWeight(qw.packed.clone(), qw.scales.clone(), K, N, bits)
+                     for _ in range(max(0, (3 * 135_000_000) // nbytes))]
+    for T in Ts:
+        x = torch.randn((T, K), generator=g, device=dev).to(torch.bfloat16)
+        y = torch.empty((T, N), dtype=torch.float32, device=dev)
+        for i in range(3):
+            copies[i % len(copies)].gemv(x, y)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(reps):
+            copies[i % len(copies)].gemv(x, y)
+        e1.record()
+        torch.cuda.synchronize()
+        rc = nqp.last_device_error()
+        if rc != 0:
+            raise RuntimeError(f"device status {rc}")
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        peak, kind = measured_peaks()
+        print(json.dumps({"shape": {"K": K, "N": N, "bits": bits, "T": T}, "us_per_launch": round(us, 2),
+                          "gbs": round(nbytes / us / 1e3, 1), "frac_of_measured_hbm": round(nbytes / us / 1e3 / peak, 4),
+                          "frac_of_8tbs": round(nbytes / us / 1e3 / 8000.0, 4), "weight_bytes": nbytes,
+                          "copies": len(copies), "plan": nqp.plan(K, N, T, bits)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -429,7 +485,13 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=2.0)
+    ap.add_argument("--single", default=None,
+                    help='time one shape "K,N,bits,T" or a config name (%s)' % ", ".join(CONFIG_SHAPES))
+    ap.add_argument("--reps", type=int, default=50)
     args = ap.parse_args()
+    if args.single:
+        run_single(args.single, args.reps, args.seed)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
