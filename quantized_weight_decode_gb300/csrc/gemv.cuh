@@ -59,7 +59,7 @@ constexpr int kStatusTimeout = -5;
 // x in shared memory, kNtokXreg (MMA, one token block, x in registers, at
 // most kXregMaxGroups groups per warp slice), FMA route: NTOK = max tokens.
 constexpr int kNtokXreg = 3;
-constexpr int kXregMaxGroups = 6;
+constexpr int kXregMaxGroups = 6;  // (slice_xr dispatch covers 1..6)
 // kNtokXreg2: two token blocks (T <= 16), x in registers, at most
 // kXreg2MaxGroups groups per warp slice.
 constexpr int kNtokXreg2 = 4;
@@ -474,6 +474,19 @@ __device__ __forceinline__ bool hand_partial_mma(const GemvArgs& a, uint8_t* sme
   return true;
 }
 
+// NG consecutive groups of a warp slice, unrolled without branches.
+template <int BITS, int NT, int GWM, int NG>
+__device__ __forceinline__ void slice_xr(const uint8_t* codes, const uint8_t* scales,
+                                         const uint32_t (&xr)[GWM][NT][8], int lane, int q,
+                                         float (&acc)[NT][4]) {
+  if constexpr (NG <= GWM) {
+#pragma unroll
+    for (int i = 0; i < NG; ++i)
+      mma_group_xr<BITS, NT>(codes + i * (128 * BITS), scales + i * kScaleBytesPerBlock, xr[i],
+                             lane, q, acc);
+  }
+}
+
 // x in registers: a stage holds the CTA's whole K range of one job; the warp
 // decodes its fixed slice of it (at most GWM groups) against x fragments of
 // NT token blocks loaded once per kernel.
@@ -520,11 +533,17 @@ __device__ void consumer_xreg(const GemvArgs& a, uint8_t* smem, const Bars& bars
     for (int nb = 0; nb < NT; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
     if (!wt.wait_warp<false>(bars.full(stage), phase)) return;
     const uint8_t* st = ring + stage * a.stage_bytes;
-#pragma unroll
-    for (int i = 0; i < GWM; ++i)
-      if (i < n)
-        mma_group_xr<BITS, NT>(st + codes_off + i * kBlock,
-                               st + scales_off + i * kScaleBytesPerBlock, xr[i], lane, q, acc);
+    // One straight-line body per slice length (uniform per warp), so the
+    // compiler can overlap one group's decode with the previous group's MMAs.
+    switch (n) {
+      case 1: slice_xr<BITS, NT, GWM, 1>(st + codes_off, st + scales_off, xr, lane, q, acc); break;
+      case 2: slice_xr<BITS, NT, GWM, 2>(st + codes_off, st + scales_off, xr, lane, q, acc); break;
+      case 3: slice_xr<BITS, NT, GWM, 3>(st + codes_off, st + scales_off, xr, lane, q, acc); break;
+      case 4: slice_xr<BITS, NT, GWM, 4>(st + codes_off, st + scales_off, xr, lane, q, acc); break;
+      case 5: slice_xr<BITS, NT, GWM, 5>(st + codes_off, st + scales_off, xr, lane, q, acc); break;
+      case 6: slice_xr<BITS, NT, GWM, 6>(st + codes_off, st + scales_off, xr, lane, q, acc); break;
+      default: break;
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.empty(stage));
     if (++stage == a.stages) { stage = 0; phase ^= 1; }
