@@ -162,6 +162,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+# ------------------------------------------------------------------ multi-rank helpers
+def max_over_ranks(value: float, device=None) -> float:
+    """The maximum of a per-rank float over the default process group; the
+    value itself when no group is initialised (N = 1)."""
+    import torch
+    import torch.distributed as td
+    if not (td.is_available() and td.is_initialized()) or td.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    td.all_reduce(t, op=td.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, steps: int, bytes_per_step: int, ms: float) -> float:
+    """Whole-job throughput: every rank streams ``bytes_per_step`` per step
+    (replicas, weak scaling), divided by the slowest rank's time."""
+    return world * steps * bytes_per_step / (ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ CPU oracle leg
 def oracle_sample(seconds: float, seed: int = 77):
     """Time the CPU oracle (fp64) on sampled rows of the same workload: rows of
@@ -327,11 +346,7 @@ def run_ours(args, rank, world, local_rank):
     rc = nqp.last_device_error(stream)
     if rc != 0:
         raise RuntimeError(f"device status {rc} in timed region")
-    total_ms = start.elapsed_time(end)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        td.all_reduce(t, op=td.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(start.elapsed_time(end), dev)
 
     # per-(T, kind) durations from consecutive events
     seg = {key: 0.0 for key in graphs}
@@ -364,18 +379,14 @@ def run_ours(args, rank, world, local_rank):
                 y_host[T].copy_(ys["head"][:T], non_blocking=True)
         e1.record(stream)
     stream.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        td.all_reduce(t, op=td.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
 
     if rank != 0:
         return
     peak, peak_kind = measured_peaks()
     steps = args.steps
-    value = world * steps * len(TS) * PASS_BYTES / (total_ms * 1e-3) / 1e9
-    e2e_value = world * e2e_steps * len(TS) * PASS_BYTES / (e2e_ms * 1e-3) / 1e9
+    value = whole_job_gbs(world, steps, len(TS) * PASS_BYTES, total_ms)
+    e2e_value = whole_job_gbs(world, e2e_steps, len(TS) * PASS_BYTES, e2e_ms)
     per_t = {}
     for T in TS:
         ms = sum(seg[(T, k)] for k in kinds) / steps

@@ -255,38 +255,98 @@ def test_max_t_long_k():
 
 
 # ---------------------------------------------------------------- full-size shapes, sampled rows
-FULL = [
-    ("gate_up_q4", "rtn", 4, 34816, 5120, [1], 0.0),
-    ("down_q5", "uniform", 5, 5120, 17408, [1, 8], 0.01),
-    ("head_q6", "rtn", 6, 248320, 5120, [1, 2, 4, 8], 0.0),
-]
+FULL = {
+    "gate_up_q4": ("rtn", 4, 34816, 5120, [1], 0.0),
+    "down_q5": ("uniform", 5, 5120, 17408, [1, 8], 0.01),
+    "head_q6": ("rtn", 6, 248320, 5120, [1, 2, 4, 8], 0.0),
+}
+SAMPLE_ROWS = 384
+
+
+@pytest.fixture(scope="module")
+def full_cases():
+    """Full-size weights built once per module: device tensors, plus the
+    oracle's inputs for a sample of rows."""
+    out = {}
+    for name, (kind, bits, N, K, Ts, outl) in FULL.items():
+        mk = rtn_case if kind == "rtn" else uniform_case
+        case = mk((400, bits), bits, N, K, 16, outlier_frac=outl)
+        packed, sp = device_weight(nqp, torch, case, DEV)
+        rng = np.random.default_rng(7)
+        rows = np.unique(np.concatenate([[0, 1, 15, 16, N // 2, N - 17, N - 1],
+                                         rng.choice(N, SAMPLE_ROWS, replace=False)]))
+        sub = dict(case, w=case["w"][rows])
+        if kind == "uniform":
+            sub["flips"] = case["flips"][rows]
+            sub["codes"] = case["codes"][rows]
+        codes, sb = oracle_inputs(sub)
+        del case["w"]
+        out[name] = {"case": case, "packed": packed, "sp": sp, "rows": rows, "codes": codes,
+                     "sb": sb, "Ts": Ts}
+    return out
+
+
+def _check_rows(fc, y, T):
+    y_ref, e_ref = oracle.gemv(fc["codes"], fc["sb"], fc["case"]["xb"][:T])
+    v = oracle.max_violation(y[:, fc["rows"]], y_ref, e_ref)
+    assert v <= 1.0, (T, v)
+    assert np.isfinite(y).all()
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name,kind,bits,N,K,Ts,outl", FULL)
-def test_full_size_sampled(name, kind, bits, N, K, Ts, outl):
-    T = max(Ts)
-    mk = rtn_case if kind == "rtn" else uniform_case
-    case = mk((400, bits), bits, N, K, T, outlier_frac=outl)
-    packed, sp = device_weight(nqp, torch, case, DEV)
-    case_w = case.pop("w")
-    rng = np.random.default_rng(7)
-    rows = np.unique(np.concatenate([[0, 1, 15, 16, N // 2, N - 17, N - 1],
-                                     rng.choice(N, 384, replace=False)]))
-    case["w"] = case_w[rows]
-    sub = dict(case)
-    if kind == "uniform":
-        sub["flips"] = case["flips"][rows]
-        sub["codes"] = case["codes"][rows]
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_sampled(full_cases, name):
+    fc = full_cases[name]
+    case = fc["case"]
+    K, N, bits = case["K"], case["N"], case["bits"]
     # dequant of the sampled rows is bit-exact
-    wd = nqp.dequant(packed, sp, K, N, bits)
-    codes, sb = oracle_inputs(sub)
-    assert np.array_equal(wd[torch.from_numpy(rows).to(DEV)].cpu().numpy().view(np.uint32),
-                          oracle.dequant_f32(codes, sb).view(np.uint32))
+    wd = nqp.dequant(fc["packed"], fc["sp"], K, N, bits)
+    assert np.array_equal(wd[torch.from_numpy(fc["rows"]).to(DEV)].cpu().numpy().view(np.uint32),
+                          oracle.dequant_f32(fc["codes"], fc["sb"]).view(np.uint32))
     del wd
-    for t in Ts:
-        y = _y(case, packed, sp, T=t)
-        y_ref, e_ref = oracle.gemv(codes, sb, case["xb"][:t])
-        v = oracle.max_violation(y[:, rows], y_ref, e_ref)
-        assert v <= 1.0, (name, t, v)
-        assert np.isfinite(y).all()
+    for t in fc["Ts"]:
+        _check_rows(fc, _y(case, fc["packed"], fc["sp"], T=t), t)
+
+
+@pytest.mark.slow
+def test_full_size_graph_launch_path(full_cases):
+    """The launch configuration the benchmark times: back-to-back GEMVs of the
+    three full-size shapes at T = 1, 8, 16 on a side stream, captured into one
+    CUDA graph (programmatic dependent launch between the kernels), replayed
+    twice; sampled rows of every output against the oracle, and the two
+    replays bitwise equal."""
+    stream = torch.cuda.Stream(device=DEV)
+    jobs = []
+    for name in FULL:
+        fc = full_cases[name]
+        case = fc["case"]
+        x16 = device_x(torch, case, DEV)
+        for T in (1, 8, 16):
+            y = torch.full((T, case["N"]), float("nan"), dtype=torch.float32, device=DEV)
+            jobs.append((fc, x16[:T].contiguous(), y, T))
+
+    def run():
+        for fc, x, y, T in jobs:
+            c = fc["case"]
+            nqp.gemv(fc["packed"], fc["sp"], x, y, c["K"], c["N"], T, c["bits"], stream=stream)
+
+    with torch.cuda.stream(stream):
+        run()                      # plans and kernel attributes set before capture
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run()
+    outs = []
+    for _ in range(2):
+        for _, _, y, _ in jobs:
+            y.fill_(float("nan"))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+        assert nqp.last_device_error() == 0
+        outs.append([y.cpu().numpy() for _, _, y, _ in jobs])
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(a, b)
+    for (fc, _, _, T), y in zip(jobs, outs[0]):
+        _check_rows(fc, y, T)
