@@ -4,10 +4,10 @@
 Workload: the per-token MLP + head weight stream of a 64-layer Qwen3.8-27B-
 shaped model -- per layer a fused gate+up GEMV (4-bit, K=5120, N=34816) and a
 down GEMV (K=17408, N=5120; 5-bit for layers 0-35, 4-bit for 36-63), then the
-6-bit output head (K=5120, N=248320) -- run at T = 1, 8 and 16 tokens.
+6-bit output head (K=5120, N=248320) -- run at T = 1, 4, 8 and 16 tokens.
 Weights are seeded N(0, 0.02) draws encoded round-to-nearest on the device;
 x is seeded N(0, 1) in bf16.  A step is one pass over the whole stack at each
-T (3 x 129 GEMVs, 31.5 GB of packed weights), inputs resident in HBM.
+T (4 x 129 GEMVs, 41.9 GB of packed weights), inputs resident in HBM.
 
 The GEMVs of a pass are independent (no activation between them), so each
 pass is grouped by tensor kind: the 64 gate+up GEMVs, the 64 down GEMVs, the
@@ -41,7 +41,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 HIDDEN, INTER, VOCAB, LAYERS = 5120, 17408, 248320, 64
-TS = (1, 8, 16)
+TS = (1, 4, 8, 16)
 METRIC = "quantized GEMV weight-stream GB/s and % of GB300 HBM peak, T=1/8/16"
 UNIT = "GB/s"
 
@@ -68,7 +68,7 @@ KIND_BYTES = {k: sum(packed_bytes(b, K, N) for (kk, _, b, K, N) in stack_tensors
 CONFIG = {
     "workload": "64-layer Qwen3.8-27B-shaped MLP+head weight stream: per layer gate+up Q4 "
                 "5120x34816 and down 17408x5120 (Q5 layers 0-35, Q4 36-63), then the Q6 head "
-                "5120x248320; T=1/8/16; group 64, FP16 scales",
+                "5120x248320; T=1/4/8/16; group 64, FP16 scales",
     "T": list(TS),
     "weight_bytes_per_pass": PASS_BYTES,
     "l2": "inputs larger than L2 (10.49 GB of distinct packed weights per pass, L2 129 MB)",
@@ -184,7 +184,7 @@ def whole_job_gbs(world: int, steps: int, bytes_per_step: int, ms: float) -> flo
 # ------------------------------------------------------------------ CPU oracle leg
 def oracle_sample(seconds: float, seed: int = 77):
     """Time the CPU oracle (fp64) on sampled rows of the same workload: rows of
-    the gate+up, down and head tensors at T = 1, 8, 16, in proportion to their
+    the gate+up, down and head tensors at T = 1, 4, 8, 16, in proportion to their
     bytes.  Returns (GB/s of packed-weight bytes, bytes, seconds, description)."""
     import oracle
     import synth
@@ -207,7 +207,7 @@ def oracle_sample(seconds: float, seed: int = 77):
         if el >= seconds:
             break
     desc = (f"oracle.gemv (fp64, single thread) on {reps} rounds of sampled rows "
-            f"(gate+up 96 rows, down 16 rows, head 64 rows) at T=1,8,16")
+            f"(gate+up 96 rows, down 16 rows, head 64 rows) at T=1,4,8,16")
     return done_bytes / el / 1e9, done_bytes, el, desc
 
 

@@ -29,11 +29,15 @@
 // number of requests per microsecond, so small per-warp copies cap the
 // stream well below the HBM rate.  Work split: a persistent grid of clusters
 // of KS CTAs; cluster c owns a contiguous range of 16-row tiles ("jobs");
-// rank q handles groups [q G / KS, (q+1) G / KS) of every job.  For T <= 8
-// each consumer warp owns a fixed slice of those groups and keeps its x
-// fragments in registers ("x in registers"); otherwise the CTA's x slice
-// sits in shared memory, permuted into B-fragment order, and the warps take
-// the groups of a stage in turn.  Every wait is bounded by a time limit; on
+// rank q handles groups [q G / KS, (q+1) G / KS) of every job.  When the
+// slices are short (up to 5 groups per warp for T <= 8, 3 for T <= 16) each
+// consumer warp owns a fixed slice of those groups and keeps its x fragments
+// in registers ("x in registers"); otherwise the CTA's x slice sits in shared
+// memory, permuted into B-fragment order, and the warps take the groups of a
+// stage in turn.  With x in registers, 4-bit codes take an fp16 route: x is
+// staged once as fp16 scaled by a power of two per token (exact, checked;
+// else the bf16 route), which lets the decode reach two nibbles per half
+// without a shift.  Every wait is bounded by a time limit; on
 // expiry the kernel records NQ_ETIMEOUT in the status word and winds down
 // without hanging or leaving bulk copies in flight.
 #pragma once
@@ -59,7 +63,7 @@ constexpr int kStatusTimeout = -5;
 // x in shared memory, kNtokXreg (MMA, one token block, x in registers, at
 // most kXregMaxGroups groups per warp slice), FMA route: NTOK = max tokens.
 constexpr int kNtokXreg = 3;
-constexpr int kXregMaxGroups = 6;  // (slice_xr dispatch covers 1..6)
+constexpr int kXregMaxGroups = 5;  // (the slice-length dispatch covers 1..5)
 // kNtokXreg2: two token blocks (T <= 16), x in registers, at most
 // kXreg2MaxGroups groups per warp slice.
 constexpr int kNtokXreg2 = 4;
@@ -80,6 +84,9 @@ struct GemvArgs {
   int stages;              // ring depth
   int stage_bytes;         // bytes of one stage (codes, then scales; 128-aligned)
   int off_ring, off_red, off_cl, off_x;  // shared-memory offsets
+  int off_xh;              // fp16 x staging (4-bit codes, x in registers) at the ring's
+                           // tail, or -1: no fp16 route
+  int xh_stage0;           // first ring stage overlapping that staging area
   int nbuf;                // partial-sum buffers in flight (<= kMaxBufs)
   unsigned long long wait_ns;
   int* status;
@@ -97,8 +104,12 @@ struct Bars {
 };
 constexpr int kAbortFlagOffset = 8 * (2 * kMaxStages + 4 * kMaxBufs);
 constexpr int kZeroAreaOffset = kAbortFlagOffset + 32;  // 32 zero bytes: x of absent tokens
+constexpr int kXFreeBarOffset = kZeroAreaOffset + 32;   // mbarrier: consumers done with x staging
+// fp16 x staging statistics: [t] largest |x| bit pattern of token t, [16 + t]
+// smallest nonzero one, [32] set when some token cannot take the fp16 route.
+constexpr int kXStatOffset = kXFreeBarOffset + 64;
 constexpr int kBarRegionBytes = 1024;
-static_assert(kZeroAreaOffset + 32 <= kBarRegionBytes, "barrier region");
+static_assert(kXStatOffset + 33 * 4 <= kBarRegionBytes, "barrier region");
 
 struct Waiter {
   volatile int* abort;
@@ -184,11 +195,20 @@ __device__ void producer(const GemvArgs& a, uint8_t* smem, const Bars& bars, con
   uint32_t phase = 0;
   uint32_t issued = 0, last_par = 0;  // per-stage bookkeeping for the wind-down
   bool ok = true;
+  // Stages from xh_stage0 on share their bytes with the consumers' fp16 x
+  // staging: their first fill waits until every consumer warp has taken its
+  // x fragments (the fence orders those generic accesses before the copies).
+  bool x_pending = a.off_xh >= 0;
   for (int j = 0; j < wk.njobs && ok; ++j) {
     const long long blk_job = (wk.rt_begin + j) * a.G;
     for (int g0 = wk.g_begin; g0 < wk.g_end; g0 += sg) {
       const int ng = min(sg, wk.g_end - g0);
       if (!wt.wait<false>(bars.empty(stage), phase ^ 1)) { ok = false; break; }
+      if (x_pending && stage >= a.xh_stage0) {
+        if (!wt.wait<false>(smem_addr(smem + kXFreeBarOffset), 0)) { ok = false; break; }
+        fence_proxy_async_smem();
+        x_pending = false;
+      }
       const uint32_t bc = static_cast<uint32_t>(ng * kBlock);
       const uint32_t bs = static_cast<uint32_t>(ng * kScaleBytesPerBlock);
       const uint32_t dst = ring + stage * a.stage_bytes;
@@ -320,6 +340,27 @@ __device__ __forceinline__ uint32_t pair_codes_bf16(const uint32_t (&w)[BITS], i
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
+// fp16 route for 4-bit codes (x in registers, converted once to fp16): with
+// exponent 2^10 the 10-bit fp16 mantissa holds a nibble at bits 0-3 or at
+// bits 4-7 of each half as it lies: (w & 0x000F000F) | 1024 = 1024 + u and
+// (w & 0x00F000F0) | 1024 = 1024 + 16 u.  One shift by 8 serves the other two
+// nibbles of the word (the bf16 route needs three shifts per word).
+// Subtracting 1024 + 8, resp. 1024 + 128, leaves c and 16 c, exact in fp16.
+// The nibbles at offsets 4 and 12 are pairs 1 and 3 of the word -- rows q + 8
+// of the tile -- so those rows leave the MMA multiplied by 16, which the warp
+// undoes exactly (a power of two) when it hands its partial over.
+__device__ __forceinline__ void q4_codes_f16(uint32_t w, uint32_t& a0, uint32_t& a1,
+                                             uint32_t& a2, uint32_t& a3) {
+  constexpr uint32_t kMagic = 0x64006400u;  // 1024
+  constexpr uint32_t kLo = 0x64086408u;     // 1024 + 8
+  constexpr uint32_t kHi = 0x64806480u;     // 1024 + 128
+  const uint32_t w8 = w >> 8;
+  a0 = sub_f16x2(lop3_and_or(w, 0x000F000Fu, kMagic), kLo);
+  a1 = sub_f16x2(lop3_and_or(w, 0x00F000F0u, kMagic), kHi);
+  a2 = sub_f16x2(lop3_and_or(w8, 0x000F000Fu, kMagic), kLo);
+  a3 = sub_f16x2(lop3_and_or(w8, 0x00F000F0u, kMagic), kHi);
+}
+
 // ------------------------------------------------------------------ per-group math
 // One group of one row tile on the MMA route: decode the lane's 32 codes, four
 // chained MMAs against the x fragments (the first starts from zero), scale,
@@ -445,6 +486,37 @@ __device__ __forceinline__ void mma_group_xr(const uint8_t* blk, const uint8_t* 
   }
 }
 
+// mma_group_xr on the fp16 route (4-bit codes; xr holds fp16 x * 2^e).
+template <int NT>
+__device__ __forceinline__ void mma_group_xr_f16(const uint8_t* blk, const uint8_t* sc,
+                                                 const uint32_t (&xr)[NT][8], int lane, int q,
+                                                 float (&acc)[NT][4]) {
+  uint32_t w[4];
+  load_lane_words<4>(blk, lane, w);
+  const float2 s = __half22float2(*reinterpret_cast<const __half2*>(sc + 4 * q));
+  float d[NT][4];
+#pragma unroll
+  for (int js = 0; js < 4; ++js) {
+    uint32_t a0, a1, a2, a3;
+    q4_codes_f16(w[js], a0, a1, a2, a3);
+#pragma unroll
+    for (int nb = 0; nb < NT; ++nb) {
+      if (js == 0) {
+        mma_16816_f16_zc(d[nb], a0, a1, a2, a3, xr[nb][0], xr[nb][1]);
+      } else {
+        mma_16816_f16(d[nb], a0, a1, a2, a3, xr[nb][2 * js], xr[nb][2 * js + 1]);
+      }
+    }
+  }
+#pragma unroll
+  for (int nb = 0; nb < NT; ++nb) {
+    acc[nb][0] = fmaf(s.x, d[nb][0], acc[nb][0]);
+    acc[nb][1] = fmaf(s.x, d[nb][1], acc[nb][1]);
+    acc[nb][2] = fmaf(s.y, d[nb][2], acc[nb][2]);
+    acc[nb][3] = fmaf(s.y, d[nb][3], acc[nb][3]);
+  }
+}
+
 // ------------------------------------------------------------------ consumers
 // Hand a warp's 16 x T partial of job j to the epilogue (MMA accumulator
 // layout: lane q*4+r holds rows q, q+8 and tokens 8 nb + 2r, +1).
@@ -475,35 +547,30 @@ __device__ __forceinline__ bool hand_partial_mma(const GemvArgs& a, uint8_t* sme
 }
 
 // NG consecutive groups of a warp slice, unrolled without branches.
-template <int BITS, int NT, int GWM, int NG>
+template <int BITS, int NT, int GWM, int NG, bool F16>
 __device__ __forceinline__ void slice_xr(const uint8_t* codes, const uint8_t* scales,
                                          const uint32_t (&xr)[GWM][NT][8], int lane, int q,
                                          float (&acc)[NT][4]) {
   if constexpr (NG <= GWM) {
 #pragma unroll
-    for (int i = 0; i < NG; ++i)
-      mma_group_xr<BITS, NT>(codes + i * (128 * BITS), scales + i * kScaleBytesPerBlock, xr[i],
+    for (int i = 0; i < NG; ++i) {
+      if constexpr (F16) {
+        mma_group_xr_f16<NT>(codes + i * (128 * BITS), scales + i * kScaleBytesPerBlock, xr[i],
                              lane, q, acc);
+      } else {
+        mma_group_xr<BITS, NT>(codes + i * (128 * BITS), scales + i * kScaleBytesPerBlock, xr[i],
+                               lane, q, acc);
+      }
+    }
   }
 }
 
-// x in registers: a stage holds the CTA's whole K range of one job; the warp
-// decodes its fixed slice of it (at most GWM groups) against x fragments of
-// NT token blocks loaded once per kernel.
-template <int BITS, int GWM, int NT>
-__device__ void consumer_xreg(const GemvArgs& a, uint8_t* smem, const Bars& bars,
-                              const Waiter& wt, const Work& wk, int warp, int lane) {
-  constexpr int kBlock = 128 * BITS;
+// The lane's x fragments of the warp slice (groups i < n, tokens < T; zeros
+// elsewhere), as bf16 pairs straight from x.
+template <int GWM, int NT>
+__device__ __forceinline__ void load_x_frags(const GemvArgs& a, const Slice& sl, int n, int lane,
+                                             uint32_t (&xr)[GWM][NT][8]) {
   const int q = lane >> 2, r = lane & 3;
-  const int T = a.T;
-  const Slice sl = warp_slice(wk, warp);
-  const int n = sl.ge - sl.gs;  // <= GWM
-  const int rel = sl.gs - wk.g_begin;
-  const uint8_t* ring = smem + a.off_ring;
-  const int codes_off = rel * kBlock;
-  const int scales_off = a.stage_groups * kBlock + rel * kScaleBytesPerBlock;
-
-  uint32_t xr[GWM][NT][8];
 #pragma unroll
   for (int i = 0; i < GWM; ++i) {
 #pragma unroll
@@ -511,7 +578,7 @@ __device__ void consumer_xreg(const GemvArgs& a, uint8_t* smem, const Bars& bars
 #pragma unroll
       for (int e = 0; e < 8; ++e) xr[i][nb][e] = 0u;
       const int tok = 8 * nb + q;
-      if (i < n && tok < T) {
+      if (i < n && tok < a.T) {
         const uint32_t* src = reinterpret_cast<const uint32_t*>(
             a.x + static_cast<long long>(tok) * a.K + 64LL * (sl.gs + i) + 2 * r);
 #pragma unroll
@@ -522,7 +589,114 @@ __device__ void consumer_xreg(const GemvArgs& a, uint8_t* smem, const Bars& bars
       }
     }
   }
+}
 
+// fp16 route of 4-bit codes (taken for T <= 2, where staging x costs less
+// than the shorter decode saves): the consumer warps stage the CTA's x range
+// once, as fp16 pairs of x * 2^e_t with one power of two e_t per token t, in
+// B-fragment order (the layout of stage_x_bf16) at off_xh.  e_t puts the
+// token's largest |x| in [2^14, 2^15); every bf16 value then converts
+// exactly when none lies more than 31 binades below it (fp16 keeps 11
+// significant bits down to 2^-14 and steps of 2^-24 below), the maximum lies
+// in [2^-100, 2^101) and nothing is subnormal, infinite or NaN.  Pass 1
+// gathers each token's largest and smallest nonzero |x|, pass 2 converts.
+// Returns, the same in every consumer thread, whether every token qualified;
+// if not, the caller takes the bf16 route and the staging area is unused.
+__device__ __forceinline__ int f16_exponent(uint32_t max_bits) {
+  return max_bits == 0 ? 0 : 141 - static_cast<int>(max_bits >> 7);
+}
+__device__ inline bool stage_x_f16(const GemvArgs& a, uint8_t* smem, const Work& wk, int warp,
+                                   int lane) {
+  const int gc = wk.g_end - wk.g_begin;
+  const int T = a.T;
+  uint32_t* stat = reinterpret_cast<uint32_t*>(smem + kXStatOffset);
+  const int per_tok = gc * 4;        // units of 16 values per token
+  const int units = T * per_tok;     // unit u: token u / per_tok, group g, slice j
+  auto src_of = [&](int u, int& tok, int& g, int& j) {
+    tok = u / per_tok;
+    const int rem = u - tok * per_tok;
+    g = rem >> 2;
+    j = rem & 3;
+    return reinterpret_cast<const uint4*>(a.x + static_cast<long long>(tok) * a.K +
+                                          64LL * (wk.g_begin + g) + 16 * j);
+  };
+  // Pass 1: per token, the largest and the smallest nonzero magnitude
+  // (bf16 magnitudes order like unsigned integers; zeros count as 0x7FFF).
+  for (int base = warp * 32; base < units; base += kWarps * 32) {
+    const int u = base + lane;
+    uint32_t mx = 0, mn = 0x7FFF7FFFu;
+    int tok = T;
+    if (u < units) {
+      int g, j;
+      const uint4* src = src_of(u, tok, g, j);
+      const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t m = w[k] & 0x7FFF7FFFu;
+        mx = __vmaxu2(mx, m);
+        mn = __vminu2(mn, m | (__vcmpeq2(m, 0u) & 0x7FFF7FFFu));
+      }
+    }
+    mx = max(mx & 0xFFFFu, mx >> 16);
+    mn = min(mn & 0xFFFFu, mn >> 16);
+    const unsigned same = __match_any_sync(0xffffffffu, tok);
+    mx = __reduce_max_sync(same, mx);
+    mn = __reduce_min_sync(same, mn);
+    if (tok < T && lane == __ffs(same) - 1) {
+      atomicMax(stat + tok, mx);
+      atomicMin(stat + 16 + tok, mn);
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+  // Pass 2: qualify each token, convert (the reloads hit L1).
+  uint8_t* xs = smem + a.off_xh;
+  for (int u = warp * 32 + lane; u < units; u += kWarps * 32) {
+    int tok, g, j;
+    const uint4* src = src_of(u, tok, g, j);
+    const uint32_t mxb = stat[tok], mnb = stat[16 + tok];
+    const int E = static_cast<int>(mxb >> 7), Emin = static_cast<int>(mnb >> 7);
+    const bool ok = mxb == 0 || (E >= 27 && E <= 227 && Emin >= 1 && Emin >= E - 31);
+    if (!ok) {
+      stat[32] = 1u;
+      continue;
+    }
+    const float sc = __int_as_float((127 + f16_exponent(mxb)) << 23);
+    const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      h[k] = cvt_f16x2(__uint_as_float(w[k] << 16) * sc, __uint_as_float(w[k] & 0xFFFF0000u) * sc);
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+      *reinterpret_cast<uint2*>(xs + ((g * T + tok) * 4 + r) * 32 + 8 * j) =
+          make_uint2(h[r], h[4 + r]);
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+  return stat[32] == 0u;
+}
+
+// The job loop of the x-in-registers consumer: per job, wait for the stage,
+// run the warp's slice (n groups, one straight-line body per slice length,
+// so the compiler can overlap one group's decode with the previous group's
+// MMAs), release the stage, hand the partial over.  F16: fp16 route; the
+// partial is brought back to the scale of x (inv) and rows q + 8 divided by
+// 16 before it is handed over.
+template <int BITS, int GWM, int NT, bool F16>
+__device__ __forceinline__ void xreg_jobs(const GemvArgs& a, uint8_t* smem, const Bars& bars,
+                                          const Waiter& wt, const Work& wk, int warp, int lane,
+                                          int n, int codes_off, int scales_off,
+                                          const uint32_t (&xr)[GWM][NT][8],
+                                          const float (&inv)[NT][2]) {
+  const int q = lane >> 2;
+  const uint8_t* ring = smem + a.off_ring;
+  float inv16[NT][2];
+#pragma unroll
+  for (int nb = 0; nb < NT; ++nb) {
+    inv16[nb][0] = inv[nb][0] * 0.0625f;
+    inv16[nb][1] = inv[nb][1] * 0.0625f;
+  }
   int stage = 0;
   uint32_t phase = 0;
   int rb = 0;        // partial buffer of this job
@@ -533,23 +707,101 @@ __device__ void consumer_xreg(const GemvArgs& a, uint8_t* smem, const Bars& bars
     for (int nb = 0; nb < NT; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
     if (!wt.wait_warp<false>(bars.full(stage), phase)) return;
     const uint8_t* st = ring + stage * a.stage_bytes;
-    // One straight-line body per slice length (uniform per warp), so the
-    // compiler can overlap one group's decode with the previous group's MMAs.
+    const uint8_t* cs = st + codes_off;
+    const uint8_t* ss = st + scales_off;
     switch (n) {
-      case 1: slice_xr<BITS, NT, GWM, 1>(st + codes_off, st + scales_off, xr, lane, q, acc); break;
-      case 2: slice_xr<BITS, NT, GWM, 2>(st + codes_off, st + scales_off, xr, lane, q, acc); break;
-      case 3: slice_xr<BITS, NT, GWM, 3>(st + codes_off, st + scales_off, xr, lane, q, acc); break;
-      case 4: slice_xr<BITS, NT, GWM, 4>(st + codes_off, st + scales_off, xr, lane, q, acc); break;
-      case 5: slice_xr<BITS, NT, GWM, 5>(st + codes_off, st + scales_off, xr, lane, q, acc); break;
-      case 6: slice_xr<BITS, NT, GWM, 6>(st + codes_off, st + scales_off, xr, lane, q, acc); break;
+      case 1: slice_xr<BITS, NT, GWM, 1, F16>(cs, ss, xr, lane, q, acc); break;
+      case 2: slice_xr<BITS, NT, GWM, 2, F16>(cs, ss, xr, lane, q, acc); break;
+      case 3: slice_xr<BITS, NT, GWM, 3, F16>(cs, ss, xr, lane, q, acc); break;
+      case 4: slice_xr<BITS, NT, GWM, 4, F16>(cs, ss, xr, lane, q, acc); break;
+      case 5: slice_xr<BITS, NT, GWM, 5, F16>(cs, ss, xr, lane, q, acc); break;
       default: break;
     }
+    static_assert(GWM <= 5, "slice-length dispatch covers 1..5 groups");
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.empty(stage));
     if (++stage == a.stages) { stage = 0; phase ^= 1; }
+    if constexpr (F16) {
+#pragma unroll
+      for (int nb = 0; nb < NT; ++nb) {
+        acc[nb][0] *= inv[nb][0];
+        acc[nb][1] *= inv[nb][1];
+        acc[nb][2] *= inv16[nb][0];
+        acc[nb][3] *= inv16[nb][1];
+      }
+    }
     if (!hand_partial_mma<NT>(a, smem, bars, wt, warp, lane, rb, rn, acc)) return;
     if (++rb == a.nbuf) { rb = 0; ++rn; }
   }
+}
+
+// x in registers: a stage holds the CTA's whole K range of one job; the warp
+// decodes its fixed slice of it (at most GWM groups) against x fragments of
+// NT token blocks loaded once per kernel.  4-bit codes take the fp16 route
+// when x converts exactly (see stage_x_f16), every other case the bf16 route.
+template <int BITS, int GWM, int NT>
+__device__ void consumer_xreg(const GemvArgs& a, uint8_t* smem, const Bars& bars,
+                              const Waiter& wt, const Work& wk, int warp, int lane) {
+  constexpr int kBlock = 128 * BITS;
+  const Slice sl = warp_slice(wk, warp);
+  const int n = sl.ge - sl.gs;  // <= GWM
+  const int rel = sl.gs - wk.g_begin;
+  const int codes_off = rel * kBlock;
+  const int scales_off = a.stage_groups * kBlock + rel * kScaleBytesPerBlock;
+
+  uint32_t xr[GWM][NT][8];
+  float inv[NT][2];
+  if constexpr (BITS == 4) {
+    if (a.off_xh >= 0) {
+      const bool f16 = stage_x_f16(a, smem, wk, warp, lane);
+      if (f16) {
+        // Fragments from the staging area; inv: 2^-e_t of this lane's
+        // accumulator columns (tokens 8 nb + 2r + c).
+        const int q = lane >> 2, r = lane & 3;
+        const uint32_t* stat = reinterpret_cast<const uint32_t*>(smem + kXStatOffset);
+#pragma unroll
+        for (int nb = 0; nb < NT; ++nb) {
+          const int tok = 8 * nb + q;
+#pragma unroll
+          for (int i = 0; i < GWM; ++i) {
+            uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+            if (i < n && tok < a.T) {
+              const uint8_t* p = smem + a.off_xh + (((rel + i) * a.T + tok) * 4 + r) * 32;
+              v0 = *reinterpret_cast<const uint4*>(p);
+              v1 = *reinterpret_cast<const uint4*>(p + 16);
+            }
+            xr[i][nb][0] = v0.x; xr[i][nb][1] = v0.y; xr[i][nb][2] = v0.z; xr[i][nb][3] = v0.w;
+            xr[i][nb][4] = v1.x; xr[i][nb][5] = v1.y; xr[i][nb][6] = v1.z; xr[i][nb][7] = v1.w;
+          }
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int t = 8 * nb + 2 * r + c;
+            const int e = t < a.T ? f16_exponent(stat[t]) : 0;
+            inv[nb][c] = __int_as_float((127 - e) << 23);
+          }
+        }
+      } else {
+        load_x_frags<GWM, NT>(a, sl, n, lane, xr);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(smem + kXFreeBarOffset));
+      if (f16) {
+        xreg_jobs<BITS, GWM, NT, true>(a, smem, bars, wt, wk, warp, lane, n, codes_off,
+                                       scales_off, xr, inv);
+        return;
+      }
+#pragma unroll
+      for (int nb = 0; nb < NT; ++nb) inv[nb][0] = inv[nb][1] = 1.f;
+      xreg_jobs<BITS, GWM, NT, false>(a, smem, bars, wt, wk, warp, lane, n, codes_off, scales_off,
+                                      xr, inv);
+      return;
+    }
+  }
+  load_x_frags<GWM, NT>(a, sl, n, lane, xr);
+#pragma unroll
+  for (int nb = 0; nb < NT; ++nb) inv[nb][0] = inv[nb][1] = 1.f;
+  xreg_jobs<BITS, GWM, NT, false>(a, smem, bars, wt, wk, warp, lane, n, codes_off, scales_off, xr,
+                                  inv);
 }
 
 // x in shared memory: the warps take the groups of each stage in turn
@@ -747,6 +999,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     }
     *abort_flag = 0;
     for (int i = 0; i < 8; ++i) reinterpret_cast<uint32_t*>(smem + kZeroAreaOffset)[i] = 0u;
+    mbar_init(smem_addr(smem + kXFreeBarOffset), kWarps);
+    uint32_t* stat = reinterpret_cast<uint32_t*>(smem + kXStatOffset);
+    for (int t = 0; t < 16; ++t) {
+      stat[t] = 0u;
+      stat[16 + t] = 0x7FFFu;
+    }
+    stat[32] = 0u;
     fence_mbar_init();
   }
   // Later kernels of the stream may start their weight streaming once every

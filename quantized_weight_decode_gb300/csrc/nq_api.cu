@@ -112,9 +112,12 @@ const void* kernel_for(int bits, int route, int ntok) {
 
 int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
+constexpr int kF16MaxT = 2;  // largest T that takes the fp16 route of 4-bit codes
+
 struct Plan {
   int route = 0, ntok = 0, ks = 1, clusters = 0, sg = 1, stages = 0, stage_bytes = 0, nbuf = 2;
   int smem = 0, off_ring = 0, off_red = 0, off_cl = 0, off_x = 0;
+  int off_xh = -1, xh_stage0 = 0;  // fp16 x staging of the 4-bit x-in-register kernels
   const void* func = nullptr;
   double est_us = 0;
 };
@@ -150,6 +153,21 @@ bool layout_for(const Plan& base, int G, int T, int bits, int ks, int sg, int mi
   p.stages = static_cast<int>(std::min<long long>(kMaxStages, (smem_optin - fixed) / p.stage_bytes));
   if (p.stages < min_stages) return false;
   p.smem = p.off_ring + p.stages * p.stage_bytes;
+  // 4-bit codes with x in registers, T <= kF16MaxT: the consumers stage x
+  // once as fp16 at the tail of the ring (T x 64 values x 2 B per group),
+  // before the producer's first fill of the stages there; at least one stage
+  // stays clear of it so the stream starts at once.  (Staging costs grow
+  // with T; from T = 4 on they exceed what the shorter decode saves.)
+  p.off_xh = -1;
+  p.xh_stage0 = p.stages;
+  if (x_in_regs && bits == 4 && T <= kF16MaxT && env_int("NQ_X_F16", 1) != 0) {
+    const int xh_bytes = align_up(gc_max * T * 128, 128);
+    const int off = (p.smem - xh_bytes) / 128 * 128;
+    if (off >= p.off_ring + p.stage_bytes) {
+      p.off_xh = off;
+      p.xh_stage0 = (off - p.off_ring) / p.stage_bytes;
+    }
+  }
   *out = p;
   return true;
 }
@@ -320,6 +338,8 @@ int launch_plan(const Plan& p, const void* packed, const uint16_t* scales, const
   a.off_red = p.off_red;
   a.off_cl = p.off_cl;
   a.off_x = p.off_x;
+  a.off_xh = p.off_xh;
+  a.xh_stage0 = p.xh_stage0;
   a.nbuf = p.nbuf;
   a.wait_ns = static_cast<unsigned long long>(std::max(1, env_int("NQ_WAIT_MS", 2000))) * 1000000ULL;
   a.status = d->status;

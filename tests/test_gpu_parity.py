@@ -11,6 +11,7 @@ import torch
 
 import oracle
 import quantized_weight_decode_gb300 as nqp
+import synth
 from cases import device_weight, device_x, oracle_inputs, rtn_case, uniform_case
 
 pytestmark = pytest.mark.gpu
@@ -211,6 +212,77 @@ def test_repeat_runs_identical():
     a = _y(case, packed, sp)
     b = _y(case, packed, sp)
     assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------- fp16 route of 4-bit codes
+def _scaled_x(xb, factors):
+    """bf16 bit patterns of x[t] * factors[t] (fp32 product rounded to bf16)."""
+    xf = (xb.astype(np.uint32) << 16).view(np.float32)
+    return synth._f32_to_bf16_bits(xf * np.asarray(factors, np.float32)[:, None])
+
+
+def _x_edge_cases(xb):
+    T = xb.shape[0]
+    tiny = xb.copy()
+    tiny[T - 1, 70] = np.uint16(np.float32(2.0 ** -40).view(np.uint32) >> 16)  # ~53 binades down
+    zero = xb.copy()
+    zero[0] = 0                                                              # an all-zero token
+    return {
+        "tiny_element": tiny,                                # the CTA falls back to bf16
+        "huge": _scaled_x(xb, [2.0 ** 110] * T),             # max above 2^101: bf16 route
+        "subnormal_scale": _scaled_x(xb, [2.0 ** -118] * T),  # max below 2^-100: bf16 route
+        "token_scales": _scaled_x(xb, [2.0 ** (40 * t - 30) for t in range(T)]),
+        "zero_token": zero,
+    }
+
+
+def _check_x(case, packed, sp, xb, name):
+    c = dict(case, xb=xb)
+    y = _y(c, packed, sp, route=nqp.ROUTE_MMA)
+    assert np.isfinite(y).all(), name
+    codes, sb = oracle_inputs(c)
+    y_ref, e_ref = oracle.gemv(codes, sb, xb)
+    v = oracle.max_violation(y, y_ref, e_ref)
+    assert v <= 1.0, (name, v)
+    return y
+
+
+@pytest.mark.parametrize("T", [1, 2])
+def test_q4_f16_route_x_edge_cases(T):
+    """4-bit codes with x in registers at T <= 2 go through fp16 when every x
+    converts exactly after a per-token power-of-two scaling, else through
+    bf16; both must meet the oracle's tolerance whatever x looks like."""
+    case = rtn_case((314, T), 4, 100, 1024, T)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    assert nqp.plan(1024, 100, T, 4)["ksplit"] == 1
+    for name, xb in _x_edge_cases(case["xb"]).items():
+        _check_x(case, packed, sp, xb, name)
+
+
+@pytest.mark.parametrize("T", [1, 2])
+def test_q4_f16_and_bf16_routes_agree(T, monkeypatch):
+    """The same product through the fp16 route (default at T <= 2) and through
+    the bf16 route (NQ_X_F16=0): both within the oracle's tolerance, and
+    one-hot x gives the weight column exactly on both."""
+    case = rtn_case((315, T), 4, 2000, 5120, T)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    y16 = _check_x(case, packed, sp, case["xb"], "fp16 route")
+    monkeypatch.setenv("NQ_X_F16", "0")
+    ybf = _check_x(case, packed, sp, case["xb"], "bf16 route")
+    monkeypatch.delenv("NQ_X_F16")
+    codes, sb = oracle_inputs(case)
+    _, e_ref = oracle.gemv(codes, sb, case["xb"])
+    assert np.all(np.abs(y16 - ybf) <= 2e-4 * e_ref + 2e-6)
+    wref = oracle.dequant_f32(codes, sb)
+    xb = np.zeros((T, 5120), np.uint16)
+    for t in range(T):
+        xb[t, 777 + 1000 * t] = 0x3F80
+    for env in ("1", "0"):
+        monkeypatch.setenv("NQ_X_F16", env)
+        y = _y(dict(case, xb=xb), packed, sp)
+        for t in range(T):
+            assert np.array_equal(y[t], wref[:, 777 + 1000 * t]), (env, t)
+    monkeypatch.delenv("NQ_X_F16")
 
 
 # ---------------------------------------------------------------- errors and edge cases
