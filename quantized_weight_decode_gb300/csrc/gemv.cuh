@@ -169,15 +169,19 @@ __device__ __forceinline__ Work cta_work(const GemvArgs& a) {
 }
 
 // The fixed K slice of consumer warp `warp` (x in registers): groups
-// [gs, ge) of every job.
+// [gs, ge) of every job.  When the CTA's groups do not divide evenly, the
+// last (gc mod 16) warps take one group more: consecutive warps sit on the
+// four SM sub-partitions in turn (warp mod 4), so the extra groups spread
+// evenly over them instead of piling up on one sub-partition.
 struct Slice {
   int gs, ge;
 };
 __device__ __forceinline__ Slice warp_slice(const Work& wk, int warp) {
   const int gc = wk.g_end - wk.g_begin;
+  const int base = gc / kWarps, first_extra = kWarps - gc % kWarps;
   Slice s;
-  s.gs = wk.g_begin + (warp * gc) / kWarps;
-  s.ge = wk.g_begin + ((warp + 1) * gc) / kWarps;
+  s.gs = wk.g_begin + warp * base + max(0, warp - first_extra);
+  s.ge = s.gs + base + (warp >= first_extra ? 1 : 0);
   return s;
 }
 

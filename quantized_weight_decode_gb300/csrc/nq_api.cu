@@ -281,6 +281,14 @@ int make_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, Plan
   const int cands[4] = {1, 2, 4, 8};
   bool have = false;
   Plan best;
+  // For T <= 8 the x-in-register kernel at the smallest K split (up to 4)
+  // that allows it beats every other candidate on GB300 -- measured on the
+  // 27B shapes (K = 5120: KS 1; K = 17408: KS 4, 7-15 % ahead of KS 1/2 with
+  // x in shared memory) -- because its consumers issue the fewest
+  // instructions per weight, and the split's per-job overhead grows with KS.
+  // Larger T, or no such candidate: the time model below decides.
+  bool have_xreg = false;
+  Plan best_xreg;
   for (int ks : cands) {
     if (ksplit != 0 && ks != ksplit) continue;
     if (ks > G) continue;
@@ -309,9 +317,13 @@ int make_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, Plan
       best = p;
       have = true;
     }
+    if (!have_xreg && route == NQ_ROUTE_MMA && T <= 8 && ks <= 4 && p.func == xreg.func) {
+      best_xreg = p;
+      have_xreg = true;
+    }
   }
   if (!have) return NQ_EUNSUPPORTED;
-  *out = best;
+  *out = have_xreg ? best_xreg : best;
   return NQ_OK;
 }
 
