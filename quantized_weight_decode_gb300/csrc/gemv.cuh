@@ -902,38 +902,47 @@ __device__ void consumer_xsmem(const GemvArgs& a, uint8_t* smem, const Bars& bar
 // No cluster-scope fence is needed: the peers' data is published by the
 // transaction count of st.async, and rank 0's "slot free" signal back to a
 // peer only orders rank 0's reads, which have completed once their values
-// have been added.  Lane l handles values l, l + 32, ... of the 16 x T tile;
-// `nvi` (uniform) of the MAXV register slots are in use, so nothing is issued
-// for tokens that do not exist.
+// have been added.  Lane l handles the four consecutive values 4 l + 128 i,
+// i < SLOTS, of the 16 x T tile (value e = 16 t + row); only slots that hold
+// values are touched, so nothing is issued for tokens that do not exist.
 // Epilogue warp `ew` handles jobs ew, ew + kEpiWarps, ...; nbuf is a multiple
 // of kEpiWarps, so each partial buffer always belongs to the same warp.
-template <int MAXV>
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, const float4& v,
+                                            uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+               ::"r"(cluster_addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(cluster_bar)
+               : "memory");
+}
+__device__ __forceinline__ void add4(float4& a, const float4& b) {
+  a.x += b.x;
+  a.y += b.y;
+  a.z += b.z;
+  a.w += b.w;
+}
+template <int SLOTS>
 __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& bars,
                                 const Waiter& wt, const Work& wk, int ew, int lane) {
   const int T = a.T;
-  const int nv = 16 * T;             // values per row tile
-  const int nvi = (nv + 31) >> 5;    // value slots per lane in use (uniform)
+  const int nv = 16 * T;             // values per row tile (a multiple of 16)
   const int ks = a.ksplit;
   const float* red = reinterpret_cast<const float*>(smem + a.off_red);
   float* cl = reinterpret_cast<float*>(smem + a.off_cl);
   const uint32_t cl_bytes = static_cast<uint32_t>((ks - 1) * nv * 4);
-  // Value lane + 32 i exists iff it is < nv; nv is a multiple of 16, so only
-  // the last slot in use can be partial.
-  auto has = [&](int i) { return i < nvi && lane + 32 * i < nv; };
+  auto has = [&](int i) { return 4 * lane + 128 * i < nv; };
   int b = ew;        // buffer of job j (j % nbuf)
   uint32_t n = 0;    // uses of that buffer so far (j / nbuf)
   for (int j = ew; j < wk.njobs; j += kEpiWarps) {
     if (ks > 1 && wk.rank == 0 && lane == 0)
       mbar_arrive_expect_tx_relaxed(bars.cl_full(b), cl_bytes);
     if (!wt.wait_warp<false>(bars.red_full(b), n & 1u)) return;
-    float v[MAXV];
+    float4 v[SLOTS];
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
-      v[i] = 0.f;
+    for (int i = 0; i < SLOTS; ++i) {
+      v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (has(i)) {
-        const float* p = red + b * kWarps * nv + lane + 32 * i;
+        const float* p = red + b * kWarps * nv + 4 * lane + 128 * i;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) v[i] += p[w * nv];
+        for (int w = 0; w < kWarps; ++w) add4(v[i], *reinterpret_cast<const float4*>(p + w * nv));
       }
     }
     // Every lane has consumed its loads of the slot (the sums above); a
@@ -944,19 +953,19 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
       if (wk.rank != 0) {
         if (!wt.wait_warp<false>(bars.cl_empty(b), (n & 1u) ^ 1u)) return;
         const uint32_t dst0 =
-            map_to_rank(smem_addr(cl + (b * (ks - 1) + (wk.rank - 1)) * nv + lane), 0);
+            map_to_rank(smem_addr(cl + (b * (ks - 1) + (wk.rank - 1)) * nv + 4 * lane), 0);
         const uint32_t bar0 = map_to_rank(bars.cl_full(b), 0);
 #pragma unroll
-        for (int i = 0; i < MAXV; ++i)
-          if (has(i)) st_async_f32(dst0 + 128 * i, v[i], bar0);
+        for (int i = 0; i < SLOTS; ++i)
+          if (has(i)) st_async_v4(dst0 + 512 * i, v[i], bar0);
         store = false;
       } else {
         if (!wt.wait_warp<false>(bars.cl_full(b), n & 1u)) return;
         for (int p = 1; p < ks; ++p) {
-          const float* src = cl + (b * (ks - 1) + (p - 1)) * nv + lane;
+          const float* src = cl + (b * (ks - 1) + (p - 1)) * nv + 4 * lane;
 #pragma unroll
-          for (int i = 0; i < MAXV; ++i)
-            if (has(i)) v[i] += src[32 * i];
+          for (int i = 0; i < SLOTS; ++i)
+            if (has(i)) add4(v[i], *reinterpret_cast<const float4*>(src + 128 * i));
         }
         __syncwarp();
         if (lane == 0) {
@@ -967,11 +976,16 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
     if (store) {
       const long long row0 = (wk.rt_begin + j) * 16;
 #pragma unroll
-      for (int i = 0; i < MAXV; ++i) {
-        const int e = lane + 32 * i;
+      for (int i = 0; i < SLOTS; ++i) {
+        const int e = 4 * lane + 128 * i;
         if (has(i)) {
           const int tok = e >> 4, row = e & 15;
-          if (row0 + row < a.N) a.y[static_cast<long long>(tok) * a.N + row0 + row] = v[i];
+          float* yp = a.y + static_cast<long long>(tok) * a.N + row0 + row;
+          const long long nrow = a.N - (row0 + row);  // rows left in y from this one
+          const float vv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (c < nrow) yp[c] = vv[c];
         }
       }
     }
@@ -1027,9 +1041,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     griddep_wait();
     // Value slots per lane: 16 x T values over 32 lanes.
     if constexpr (ROUTE == kRouteMma && (NTOK == 2 || NTOK == kNtokXreg2)) {
-      epilogue<8>(a, smem, bars, wt, wk, ew, lane);
+      epilogue<2>(a, smem, bars, wt, wk, ew, lane);
     } else {
-      epilogue<4>(a, smem, bars, wt, wk, ew, lane);
+      epilogue<1>(a, smem, bars, wt, wk, ew, lane);
     }
   } else {
     griddep_wait();
