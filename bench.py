@@ -268,6 +268,43 @@ def build_stack(torch, nqp, dev, seed):
     return entries, x_arena, ys
 
 
+def fused_head_times(torch, nqp, entries, stream, reps):
+    """The output head through nq_gemv_head at every T (argmax, maximum and
+    logsumexp per token, logits not stored), one CUDA graph per T: average
+    microseconds per call and weight-stream GB/s."""
+    e = next(x for x in entries if x["kind"] == "head")
+    ws = torch.empty(nqp.head_workspace_bytes(), dtype=torch.uint8, device=e["x"].device)
+    out = {}
+    for T in TS:
+        res = [torch.empty(T, dtype=dt, device=ws.device) for dt in (torch.int32, torch.float32, torch.float32)]
+
+        def run():
+            nqp.gemv_head(e["qw"].packed, e["qw"].scales, e["x"][:T], e["K"], e["N"], T, e["bits"],
+                          workspace=ws, argmax=res[0], maxval=res[1], lse=res[2], stream=stream)
+        with torch.cuda.stream(stream):
+            run()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            run()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        out[f"T{T}"] = {"us_per_call": round(us, 2),
+                        "gbs": round(KIND_BYTES["head"] / (us * 1e-6) / 1e9, 1)}
+    rc = nqp.last_device_error(stream)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} in the fused head")
+    return out
+
+
 def capture(torch, nqp, entries, ys, T, kind, stream):
     sel = [e for e in entries if e["kind"] == kind]
 
@@ -358,6 +395,9 @@ def run_ours(args, rank, world, local_rank):
                 seg[(T, k)] += prev.elapsed_time(e)
                 prev = e
 
+    # ---------------- fused verify head (argmax, maximum, logsumexp per token)
+    head_fused = fused_head_times(torch, nqp, entries, stream, reps=max(10, min(args.steps, 50)))
+
     # ---------------- end to end: x from pinned host, logits back to pinned host
     x_host = torch.empty(x_arena.shape, dtype=x_arena.dtype, pin_memory=True)
     x_host.copy_(x_arena)
@@ -423,6 +463,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "per_T": per_t,
         "kernels": kernels,
+        "head_fused": head_fused,
         "plans": {f"{k}_T{T}": nqp.plan(e["K"], e["N"], T, e["bits"])
                   for T in TS for k in kinds
                   for e in [next(x for x in entries if x["kind"] == k)]},

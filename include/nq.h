@@ -139,6 +139,28 @@ int nq_gemv(const void* packed, const uint16_t* scales, const void* x_bf16, floa
 int nq_gemv_ex(const void* packed, const uint16_t* scales, const void* x_bf16, float* y,
                int64_t K, int64_t N, int T, int bits, int route, int ksplit, nq_stream_t stream);
 
+/* Fused verify head: the product of nq_gemv (y may be NULL: logits not
+ * stored) and, per token t < T, over the N outputs y[t, 0..N):
+ *   argmax[t] = the smallest n with y[t, n] maximal (int32; -1 if every
+ *               output is -inf), maxval[t] = that maximum,
+ *   lse[t]    = log(sum_n exp(y[t, n])), one pass (running maximum).
+ * These are the greedy-acceptance and normalisation values of a
+ * speculative-verify round over the output head: the pages "giveen/ninfer-ext"
+ * (section "Engineering", single-pass logsumexp) and "Qwen3.8-27B for NInfer
+ * on the RTX 3090" (section "Artifact": candidate top-k over the full head).
+ * argmax, maxval, lse: device arrays of T entries, written when the stream
+ * reaches the end of the call.  workspace: device scratch of at least
+ * nq_head_workspace_bytes() bytes, 16-byte aligned, owned by the caller, any
+ * contents on entry; calls sharing a workspace must be ordered (one stream).
+ * The result is deterministic: states are merged in a fixed order, and ties
+ * of the maximum go to the smallest index.  N <= 2^31 - 1. */
+int nq_gemv_head(const void* packed, const uint16_t* scales, const void* x_bf16, float* y,
+                 int64_t K, int64_t N, int T, int bits, int32_t* argmax, float* maxval,
+                 float* lse, void* workspace, size_t workspace_bytes, nq_stream_t stream);
+
+/* Bytes of workspace nq_gemv_head needs on the current device (any T, N). */
+int nq_head_workspace_bytes(size_t* bytes);
+
 /* Dequantised weights w[N, K] fp32 (device, row-major) = scale * code, exact.
  * Test aid: lets the decode path be checked bit for bit. */
 int nq_dequant(const void* packed, const uint16_t* scales, float* w, int64_t K, int64_t N,

@@ -185,6 +185,23 @@ def gemv_rows(codes_rows: np.ndarray, scale_rows: np.ndarray, x_bits: np.ndarray
 
 
 # --------------------------------------------------------------------------
+# Verify-head reductions over the outputs of one token (page "giveen/ninfer-ext",
+# section "Engineering": single-pass logsumexp; page "Qwen3.8-27B for NInfer on
+# the RTX 3090", section "Artifact": candidate top-k over the full head).
+# --------------------------------------------------------------------------
+def head_reduce(y):
+    """Per token t of y[T, N] (fp64): the argmax (first index of the largest
+    value), the largest value, and logsumexp = log(sum_n exp(y[t, n])),
+    evaluated as m + log(sum exp(y - m)) with m the maximum so no term
+    overflows."""
+    y = np.asarray(y, dtype=np.float64)
+    am = np.argmax(y, axis=1)                       # first occurrence of the maximum
+    m = y[np.arange(y.shape[0]), am]
+    lse = m + np.log(np.sum(np.exp(y - m[:, None]), axis=1))
+    return am, m, lse
+
+
+# --------------------------------------------------------------------------
 # Acceptance test on outputs: |y - y*| <= 1e-4 * E + 1e-6 per element.
 # --------------------------------------------------------------------------
 REL_TOL = 1e-4

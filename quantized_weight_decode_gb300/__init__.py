@@ -19,7 +19,8 @@ import numpy as np
 
 __all__ = [
     "NQError", "ROUTE_AUTO", "ROUTE_MMA", "ROUTE_FFMA", "lib", "lib_path", "build",
-    "packed_bytes", "pack", "unpack", "pack_device", "quantize_rtn", "gemv", "dequant",
+    "packed_bytes", "pack", "unpack", "pack_device", "quantize_rtn", "gemv", "gemv_head",
+    "head_workspace_bytes", "dequant",
     "last_device_error", "plan", "selftest_wait_timeout", "status_string", "layout_version",
     "QuantizedWeight", "EXPORTED",
 ]
@@ -43,6 +44,9 @@ _SIGS = {
     "nq_quantize_rtn": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _vp]),
     "nq_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "nq_gemv_ex": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp]),
+    "nq_gemv_head": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp,
+                            ctypes.c_size_t, _vp]),
+    "nq_head_workspace_bytes": (_i32, [_szp]),
     "nq_dequant": (_i32, [_vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "nq_last_device_error": (_i32, [_vp]),
     "nq_gemv_plan": (_i32, [_i64, _i64, _i32, _i32, _i32, _i32, _ip, _ip, _ip, _ip, _ip]),
@@ -111,8 +115,8 @@ def _stream_handle(stream) -> int | None:
     return stream.cuda_stream or None
 
 
-def _dptr(t) -> int:
-    return int(t.data_ptr())
+def _dptr(t):
+    return None if t is None else int(t.data_ptr())
 
 
 # ---------------------------------------------------------------- host side
@@ -187,6 +191,36 @@ def gemv(packed, scales, x, y, K: int, N: int, T: int, bits: int, route: int = R
         rc = lib().nq_gemv_ex(_dptr(packed), _dptr(scales), _dptr(x), _dptr(y), K, N, T, bits,
                               route, ksplit, _stream_handle(stream))
     _check(rc, "nq_gemv")
+
+
+def head_workspace_bytes() -> int:
+    """Workspace bytes nq_gemv_head needs on the current device."""
+    v = ctypes.c_size_t()
+    _check(lib().nq_head_workspace_bytes(ctypes.byref(v)), "nq_head_workspace_bytes")
+    return int(v.value)
+
+
+def gemv_head(packed, scales, x, K: int, N: int, T: int, bits: int, y=None, workspace=None,
+              argmax=None, maxval=None, lse=None, stream=None):
+    """Fused verify head: y = x W^T (stored if `y` is given) and, per token,
+    the argmax, the maximum and the logsumexp of the N outputs.  Returns
+    (argmax int32 [T], maxval fp32 [T], lse fp32 [T]) device tensors; the
+    workspace is allocated here if not passed (torch memory)."""
+    import torch
+    dev = x.device
+    if workspace is None:
+        workspace = torch.empty(head_workspace_bytes(), dtype=torch.uint8, device=dev)
+    if argmax is None:
+        argmax = torch.empty(T, dtype=torch.int32, device=dev)
+    if maxval is None:
+        maxval = torch.empty(T, dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty(T, dtype=torch.float32, device=dev)
+    _check(lib().nq_gemv_head(_dptr(packed), _dptr(scales), _dptr(x), _dptr(y), K, N, T, bits,
+                              _dptr(argmax), _dptr(maxval), _dptr(lse), _dptr(workspace),
+                              workspace.numel() * workspace.element_size(),
+                              _stream_handle(stream)), "nq_gemv_head")
+    return argmax, maxval, lse
 
 
 def dequant(packed, scales, K: int, N: int, bits: int, out=None, stream=None):

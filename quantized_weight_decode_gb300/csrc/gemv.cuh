@@ -44,6 +44,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <climits>
+#include <cmath>
 #include <cstdint>
 
 #include "layout.h"
@@ -90,7 +92,18 @@ struct GemvArgs {
   int nbuf;                // partial-sum buffers in flight (<= kMaxBufs)
   unsigned long long wait_ns;
   int* status;
+  // Fused verify head (h_ws != nullptr): per token t the argmax, the maximum
+  // and the logsumexp of y[t, 0..N), reduced through the workspace h_ws
+  // (layout: kHeadCounterBytes of counter, then one kHeadStateBytes state per
+  // (cluster, epilogue warp, token)).  y may then be null (logits not stored).
+  uint8_t* h_ws;
+  int* h_argmax;
+  float* h_max;
+  float* h_lse;
 };
+constexpr int kHeadCounterBytes = 256;
+constexpr int kHeadStateBytes = 16;
+constexpr int kHeadMaxT = 16;
 
 // Shared-memory map of the barrier region (first 1 KiB).
 struct Bars {
@@ -919,6 +932,91 @@ __device__ __forceinline__ void add4(float4& a, const float4& b) {
   a.z += b.z;
   a.w += b.w;
 }
+// ------------------------------------------------------------------ fused head
+// Running state of a softmax over logits seen so far: maximum m, sum of
+// exp(y - m), argmax a (smallest index among equal maxima).  An empty state is
+// (-inf, 0, INT_MAX).  head_merge is commutative bit for bit, so the butterfly
+// merges below leave every lane with the same state.
+__device__ __forceinline__ void head_push(float& m, float& s, int& a, float v, int idx) {
+  if (v > m) {
+    s = s * __expf(m - v) + 1.f;
+    m = v;
+    a = idx;
+  } else if (v != -INFINITY) {
+    s += __expf(v - m);
+  }
+}
+__device__ __forceinline__ void head_merge(float& m, float& s, int& a, float mo, float so, int ao) {
+  if (mo == -INFINITY && so == 0.f) return;
+  if (m == -INFINITY && s == 0.f) {
+    m = mo;
+    s = so;
+    a = ao;
+    return;
+  }
+  if (mo > m || (mo == m && ao < a)) {
+    s = s * __expf(m - mo) + so;
+    m = mo;
+    a = ao;
+  } else {
+    s = s + so * __expf(mo - m);
+  }
+}
+__device__ __forceinline__ void head_merge_lanes(float& m, float& s, int& a, int xor_mask) {
+  const float mo = __shfl_xor_sync(0xffffffffu, m, xor_mask);
+  const float so = __shfl_xor_sync(0xffffffffu, s, xor_mask);
+  const int ao = __shfl_xor_sync(0xffffffffu, a, xor_mask);
+  head_merge(m, s, a, mo, so, ao);
+}
+
+// End of a CTA's epilogue warp on the fused head: merge the four lanes of each
+// token, publish the warp's per-token states, and count the warp in; the
+// last of the clusters x kEpiWarps warps to arrive merges every state in
+// (cluster, warp) order and writes argmax, maximum and logsumexp.
+template <int SLOTS>
+__device__ void head_finish(const GemvArgs& a, const Work& wk, int ew, int lane,
+                            float (&hm)[SLOTS], float (&hs)[SLOTS], int (&ha)[SLOTS]) {
+  const int T = a.T;
+  const int entries = a.clusters * kEpiWarps;
+  const int me = (blockIdx.x / a.ksplit) * kEpiWarps + ew;
+  uint8_t* states = a.h_ws + kHeadCounterBytes;
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i) {
+    head_merge_lanes(hm[i], hs[i], ha[i], 1);
+    head_merge_lanes(hm[i], hs[i], ha[i], 2);
+    const int tok = (lane >> 2) + 8 * i;
+    if ((lane & 3) == 0 && tok < T) {
+      float4 st = make_float4(hm[i], hs[i], __int_as_float(ha[i]), 0.f);
+      *reinterpret_cast<float4*>(states + (static_cast<size_t>(me) * kHeadMaxT + tok) * kHeadStateBytes) = st;
+    }
+  }
+  __threadfence();
+  __syncwarp();
+  unsigned last = 0;
+  if (lane == 0)
+    last = atomicAdd(reinterpret_cast<unsigned*>(a.h_ws), 1u) == static_cast<unsigned>(entries - 1);
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __threadfence();
+  for (int t = 0; t < T; ++t) {
+    float m = -INFINITY, s = 0.f;
+    int am = INT_MAX;
+    for (int j = lane; j < entries; j += 32) {
+      const float4 st = __ldcg(reinterpret_cast<const float4*>(
+          states + (static_cast<size_t>(j) * kHeadMaxT + t) * kHeadStateBytes));
+      head_merge(m, s, am, st.x, st.y, __float_as_int(st.z));
+    }
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) head_merge_lanes(m, s, am, d);
+    if (lane == 0) {
+      a.h_argmax[t] = am == INT_MAX ? -1 : am;
+      a.h_max[t] = m;
+      a.h_lse[t] = m + __logf(s);
+    }
+  }
+  if (lane == 0) *reinterpret_cast<volatile unsigned*>(a.h_ws) = 0u;
+}
+
 template <int SLOTS>
 __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& bars,
                                 const Waiter& wt, const Work& wk, int ew, int lane) {
@@ -929,6 +1027,15 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
   float* cl = reinterpret_cast<float*>(smem + a.off_cl);
   const uint32_t cl_bytes = static_cast<uint32_t>((ks - 1) * nv * 4);
   auto has = [&](int i) { return 4 * lane + 128 * i < nv; };
+  const bool head = a.h_ws != nullptr;
+  float hm[SLOTS], hs[SLOTS];
+  int ha[SLOTS];
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i) {
+    hm[i] = -INFINITY;
+    hs[i] = 0.f;
+    ha[i] = INT_MAX;
+  }
   int b = ew;        // buffer of job j (j % nbuf)
   uint32_t n = 0;    // uses of that buffer so far (j / nbuf)
   for (int j = ew; j < wk.njobs; j += kEpiWarps) {
@@ -980,18 +1087,26 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
         const int e = 4 * lane + 128 * i;
         if (has(i)) {
           const int tok = e >> 4, row = e & 15;
-          float* yp = a.y + static_cast<long long>(tok) * a.N + row0 + row;
           const long long nrow = a.N - (row0 + row);  // rows left in y from this one
           const float vv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+          if (a.y != nullptr) {
+            float* yp = a.y + static_cast<long long>(tok) * a.N + row0 + row;
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            if (c < nrow) yp[c] = vv[c];
+            for (int c = 0; c < 4; ++c)
+              if (c < nrow) yp[c] = vv[c];
+          }
+          if (head) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              if (c < nrow) head_push(hm[i], hs[i], ha[i], vv[c], static_cast<int>(row0 + row + c));
+          }
         }
       }
     }
     b += kEpiWarps;
     if (b >= a.nbuf) { b -= a.nbuf; ++n; }
   }
+  if (head && (ks == 1 || wk.rank == 0)) head_finish<SLOTS>(a, wk, ew, lane, hm, hs, ha);
 }
 
 // ------------------------------------------------------------------ kernel

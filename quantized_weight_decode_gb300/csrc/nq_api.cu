@@ -327,8 +327,16 @@ int make_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, Plan
   return NQ_OK;
 }
 
+// Outputs of the fused verify head (all null for a plain GEMV).
+struct HeadOut {
+  void* ws = nullptr;
+  int32_t* argmax = nullptr;
+  float* maxval = nullptr;
+  float* lse = nullptr;
+};
+
 int launch_plan(const Plan& p, const void* packed, const uint16_t* scales, const void* x, float* y,
-                int64_t K, int64_t N, int T, cudaStream_t st) {
+                int64_t K, int64_t N, int T, cudaStream_t st, const HeadOut& head = HeadOut()) {
   DevInfo* d;
   if (int rc = dev_info(&d)) return rc;
   GemvArgs a;
@@ -355,6 +363,10 @@ int launch_plan(const Plan& p, const void* packed, const uint16_t* scales, const
   a.nbuf = p.nbuf;
   a.wait_ns = static_cast<unsigned long long>(std::max(1, env_int("NQ_WAIT_MS", 2000))) * 1000000ULL;
   a.status = d->status;
+  a.h_ws = static_cast<uint8_t*>(head.ws);
+  a.h_argmax = head.argmax;
+  a.h_max = head.maxval;
+  a.h_lse = head.lse;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.clusters * p.ks));
@@ -557,6 +569,46 @@ int nq_gemv_ex(const void* packed, const uint16_t* scales, const void* x_bf16, f
 int nq_gemv(const void* packed, const uint16_t* scales, const void* x_bf16, float* y, int64_t K,
             int64_t N, int T, int bits, nq_stream_t stream) {
   return nq_gemv_ex(packed, scales, x_bf16, y, K, N, T, bits, NQ_ROUTE_AUTO, 0, stream);
+}
+
+int nq_head_workspace_bytes(size_t* bytes) {
+  if (!bytes) return NQ_EINVAL;
+  DevInfo* d;
+  if (int rc = dev_info(&d)) return rc;
+  // one state per (cluster, epilogue warp, token); clusters <= SMs
+  *bytes = static_cast<size_t>(kHeadCounterBytes) +
+           static_cast<size_t>(d->sms) * kEpiWarps * kHeadMaxT * kHeadStateBytes;
+  return NQ_OK;
+}
+
+int nq_gemv_head(const void* packed, const uint16_t* scales, const void* x_bf16, float* y,
+                 int64_t K, int64_t N, int T, int bits, int32_t* argmax, float* maxval, float* lse,
+                 void* workspace, size_t workspace_bytes, nq_stream_t stream) {
+  if (!packed || !scales || !x_bf16 || !argmax || !maxval || !lse || !workspace) return NQ_EINVAL;
+  if (int rc = check_shape(K, N, bits)) return rc;
+  if (T < 1 || T > kMaxT) return NQ_EINVAL;
+  if (N > INT32_MAX) return NQ_EINVAL;  // row indices are int32
+  if (!aligned16(packed) || !aligned16(scales) || !aligned16(x_bf16) || !aligned16(workspace) ||
+      (y && !aligned16(y)))
+    return NQ_EALIGN;
+  size_t need = 0;
+  if (int rc = nq_head_workspace_bytes(&need)) return rc;
+  if (workspace_bytes < need) return NQ_EINVAL;
+  Plan p;
+  if (int rc = make_plan(K, N, T, bits, NQ_ROUTE_AUTO, 0, &p)) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // The arrival counter must start at zero on every call (a call that gave up
+  // on a bounded wait leaves it behind).
+  if (cudaMemsetAsync(workspace, 0, kHeadCounterBytes, st) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return NQ_ECUDA;
+  }
+  HeadOut h;
+  h.ws = workspace;
+  h.argmax = argmax;
+  h.maxval = maxval;
+  h.lse = lse;
+  return launch_plan(p, packed, scales, x_bf16, y, K, N, T, st, h);
 }
 
 int nq_gemv_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, int* route_out,

@@ -1,0 +1,158 @@
+"""GPU checks of the fused verify head (nq_gemv_head): argmax, maximum and
+logsumexp of every token's outputs, through the C ABI.
+
+Bars: the logits equal nq_gemv's bit for bit; argmax / maximum are exact with
+respect to the kernel's own logits (first index of the maximum); logsumexp
+is within 4e-5 + 1e-6 |lse| of the fp64 logsumexp of those logits (fp32
+running sums over up to a few hundred values per lane, merged in a fixed
+order); against the oracle, the argmax is a valid one (its true logit is
+within the two outputs' tolerances of the true maximum) and logsumexp is
+within the largest output tolerance (logsumexp is 1-Lipschitz in the largest
+output error) plus the same 4e-5."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_weight_decode_gb300 as nqp
+from cases import device_weight, device_x, oracle_inputs, rtn_case, uniform_case
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+LSE_ABS, LSE_REL = 4e-5, 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    nqp.build()
+    nqp.lib()
+    torch.cuda.set_device(0)
+    assert nqp.last_device_error() == 0
+
+
+def _lse64(y):
+    y = y.astype(np.float64)
+    m = y.max(axis=1)
+    return m + np.log(np.exp(y - m[:, None]).sum(axis=1))
+
+
+def _head(case, packed, sp, store_y=True, ws=None):
+    T, K, N, bits = case["T"], case["K"], case["N"], case["bits"]
+    x = device_x(torch, case, DEV)[:T].contiguous()
+    y = torch.full((T, N), float("nan"), dtype=torch.float32, device=DEV) if store_y else None
+    am, mx, lse = nqp.gemv_head(packed, sp, x, K, N, T, bits, y=y, workspace=ws)
+    assert nqp.last_device_error() == 0
+    return (None if y is None else y.cpu().numpy()), am.cpu().numpy(), mx.cpu().numpy(), lse.cpu().numpy()
+
+
+def _check_self(y, am, mx, lse):
+    """argmax / max / lse against the kernel's own logits."""
+    T = y.shape[0]
+    ref_am = np.argmax(y, axis=1)
+    assert np.array_equal(am, ref_am), (am, ref_am)
+    assert np.array_equal(mx.view(np.uint32), y[np.arange(T), am].view(np.uint32))
+    ref = _lse64(y)
+    assert np.all(np.abs(lse - ref) <= LSE_ABS + LSE_REL * np.abs(ref)), (lse, ref)
+
+
+def _check_oracle(case, am, mx, lse, rows=None):
+    codes, sb = oracle_inputs(case)
+    y_ref, e_ref = oracle.gemv(codes, sb, case["xb"][: case["T"]])
+    tol = oracle.REL_TOL * e_ref + oracle.ABS_TOL
+    a_ref, m_ref, l_ref = oracle.head_reduce(y_ref)
+    T = y_ref.shape[0]
+    t = np.arange(T)
+    # the chosen row is a maximum within the two tolerances
+    assert np.all(y_ref[t, am] >= m_ref - tol[t, am] - tol[t, a_ref]), (am, a_ref)
+    assert np.all(np.abs(mx - y_ref[t, am]) <= tol[t, am])
+    assert np.all(np.abs(lse - l_ref) <= tol.max(axis=1) + LSE_ABS + LSE_REL * np.abs(l_ref))
+
+
+SHAPES = [(6, 1024, 1000), (6, 512, 17), (4, 2048, 300), (5, 1024, 1), (6, 17408 // 4, 160),
+          (5, 17408, 100)]   # the last one runs as clusters of 4 CTAs (K split)
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 8, 9, 16])
+def test_head_matches_gemv_and_oracle(T):
+    for i, (bits, K, N) in enumerate(SHAPES):
+        case = rtn_case((500, T, i), bits, N, K, T)
+        packed, sp = device_weight(nqp, torch, case, DEV)
+        if K == 17408:
+            assert nqp.plan(K, N, T, bits)["ksplit"] > 1
+        y, am, mx, lse = _head(case, packed, sp)
+        # logits identical to the plain GEMV
+        x = device_x(torch, case, DEV)[:T].contiguous()
+        y2 = torch.full((T, N), float("nan"), dtype=torch.float32, device=DEV)
+        nqp.gemv(packed, sp, x, y2, K, N, T, bits)
+        assert np.array_equal(y.view(np.uint32), y2.cpu().numpy().view(np.uint32))
+        _check_self(y, am, mx, lse)
+        _check_oracle(case, am, mx, lse)
+
+
+def test_head_without_logits_and_repeat_calls():
+    case = uniform_case((501,), 5, 777, 2048, 8)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    ws = torch.empty(nqp.head_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    y, am, mx, lse = _head(case, packed, sp, ws=ws)
+    for _ in range(2):      # no logits stored; the workspace carries over between calls
+        _, am2, mx2, lse2 = _head(case, packed, sp, store_y=False, ws=ws)
+        assert np.array_equal(am, am2)
+        assert np.array_equal(mx.view(np.uint32), mx2.view(np.uint32))
+        assert np.array_equal(lse.view(np.uint32), lse2.view(np.uint32))
+    _check_self(y, am, mx, lse)
+
+
+def test_head_ties_go_to_the_smallest_row():
+    T, K, N, bits = 2, 1024, 300, 6
+    case = rtn_case((502,), bits, N, K, T)
+    codes, sb = oracle_inputs(case)
+    codes, sb = codes.copy(), sb.copy()
+    big = oracle.f64_to_fp16_bits(np.array([1.0]))[0]
+    for r in (37, 150, 299, 38):          # four identical rows with large positive weights
+        codes[r] = 31
+        sb[r] = big
+    hp, hs = nqp.pack(codes, sb, bits)
+    packed = torch.from_numpy(hp).to(DEV)
+    sp = torch.from_numpy(hs.view(np.int16)).to(DEV)
+    xb = np.full((T, K), 0x3F80, np.uint16)   # x = 1: those rows give 31 K, every other less
+    c2 = dict(case, xb=xb)
+    y, am, mx, _ = _head(c2, packed, sp)
+    assert am.tolist() == [37, 37]
+    assert np.all(y[:, [37, 38, 150, 299]] == y[:, [37]])
+    assert np.all(mx == 31.0 * K)
+
+
+def test_head_workspace_errors():
+    case = rtn_case((503,), 4, 64, 256, 1)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    x = device_x(torch, case, DEV)[:1].contiguous()
+    out = [torch.empty(1, dtype=torch.int32, device=DEV)] + \
+          [torch.empty(1, dtype=torch.float32, device=DEV) for _ in range(2)]
+    small = torch.empty(nqp.head_workspace_bytes() - 16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(nqp.NQError) as e:
+        nqp.gemv_head(packed, sp, x, 256, 64, 1, 4, workspace=small, argmax=out[0], maxval=out[1],
+                      lse=out[2])
+    assert e.value.code == nqp.EINVAL
+    big = torch.empty(nqp.head_workspace_bytes() + 64, dtype=torch.uint8, device=DEV)
+    with pytest.raises(nqp.NQError) as e:
+        nqp.gemv_head(packed, sp, x, 256, 64, 1, 4, workspace=big[8:], argmax=out[0],
+                      maxval=out[1], lse=out[2])
+    assert e.value.code == nqp.EALIGN
+    assert nqp.last_device_error() == 0
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("T", [1, 8])
+def test_head_full_size(T):
+    """The 248,320-row 6-bit output head: fused results against the kernel's own
+    logits (all rows), and the logits of sampled rows against the oracle."""
+    K, N, bits = 5120, 248320, 6
+    case = rtn_case((504, T), bits, N, K, T)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    y, am, mx, lse = _head(case, packed, sp)
+    _check_self(y, am, mx, lse)
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([am, rng.choice(N, 256, replace=False)]))
+    codes, sb = oracle_inputs(case, rows)
+    y_ref, e_ref = oracle.gemv(codes, sb, case["xb"][:T])
+    assert oracle.max_violation(y[:, rows], y_ref, e_ref) <= 1.0

@@ -269,3 +269,45 @@ def test_tolerance_catches_planted_mistakes(kind):
     bad = _planted(codes, sb, xb, kind)
     assert oracle.tolerance_ok(y.astype(np.float32), y, e)
     assert not oracle.tolerance_ok(bad, y, e)
+
+
+# ---------------------------------------------------------------- verify-head reductions
+def test_head_logsumexp_closed_forms():
+    # sum_{k=1..N} exp(log k) = N (N + 1) / 2
+    for n in (1, 2, 7, 1000, 248320):
+        y = np.log(np.arange(1, n + 1, dtype=np.float64))[None, :]
+        _, _, lse = oracle.head_reduce(y)
+        assert abs(lse[0] - np.log(n * (n + 1) / 2)) <= 1e-12 * max(1.0, np.log(n * n))
+    # N equal values v: v + log N; one value far above the rest: that value
+    y = np.full((1, 4096), -3.25)
+    assert abs(oracle.head_reduce(y)[2][0] - (-3.25 + np.log(4096))) <= 1e-13
+    y = np.array([[0.0, -1000.0, -2000.0, -745.0]])
+    assert oracle.head_reduce(y)[2][0] == 0.0
+
+
+def test_head_logsumexp_large_logits_do_not_overflow():
+    # a naive sum of exp would overflow fp64 here
+    y = np.array([[1000.0, 1000.0, 999.0]])
+    _, m, lse = oracle.head_reduce(y)
+    assert m[0] == 1000.0
+    assert abs(lse[0] - (1000.0 + np.log(2.0 + np.exp(-1.0)))) <= 1e-12
+
+
+def test_head_argmax_ties_take_the_first_index():
+    y = np.array([[1.0, 5.0, 2.0, 5.0, 5.0], [7.0, 7.0, 7.0, 7.0, 7.0], [-1.0, -2.0, -1.0, -3.0, -1.5]])
+    am, m, _ = oracle.head_reduce(y)
+    assert am.tolist() == [1, 0, 0]
+    assert m.tolist() == [5.0, 7.0, -1.0]
+
+
+def test_head_rows_are_independent_tokens():
+    rng = np.random.default_rng(5)
+    y = rng.standard_normal((6, 333))
+    am, m, lse = oracle.head_reduce(y)
+    for t in range(6):
+        a1, m1, l1 = oracle.head_reduce(y[t:t + 1])
+        assert am[t] == a1[0] and m[t] == m1[0] and lse[t] == l1[0]
+    # shift invariance: lse(y + c) = lse(y) + c, argmax unchanged
+    am2, _, lse2 = oracle.head_reduce(y + 123.5)
+    assert np.array_equal(am, am2)
+    assert np.all(np.abs(lse2 - (lse + 123.5)) <= 1e-12 * np.abs(lse2))
