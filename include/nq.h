@@ -153,7 +153,8 @@ int nq_gemv_ex(const void* packed, const uint16_t* scales, const void* x_bf16, f
  * nq_head_workspace_bytes() bytes, 16-byte aligned, owned by the caller, any
  * contents on entry; calls sharing a workspace must be ordered (one stream).
  * The result is deterministic: states are merged in a fixed order, and ties
- * of the maximum go to the smallest index.  N <= 2^31 - 1. */
+ * of the maximum go to the smallest index.  N <= 2^31 - 1; devices of up to
+ * 256 SMs (NQ_EUNSUPPORTED beyond). */
 int nq_gemv_head(const void* packed, const uint16_t* scales, const void* x_bf16, float* y,
                  int64_t K, int64_t N, int T, int bits, int32_t* argmax, float* maxval,
                  float* lse, void* workspace, size_t workspace_bytes, nq_stream_t stream);

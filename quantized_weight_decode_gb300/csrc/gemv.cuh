@@ -94,8 +94,10 @@ struct GemvArgs {
   int* status;
   // Fused verify head (h_ws != nullptr): per token t the argmax, the maximum
   // and the logsumexp of y[t, 0..N), reduced through the workspace h_ws
-  // (layout: kHeadCounterBytes of counter, then one kHeadStateBytes state per
-  // (cluster, epilogue warp, token)).  y may then be null (logits not stored).
+  // (layout: kHeadCounterBytes of arrival counters -- [0] all groups, [1 + g]
+  // group g -- then one kHeadStateBytes state per (cluster, epilogue warp,
+  // token), then one per (group of kHeadGroup clusters, token)).  y may then
+  // be null (logits not stored).
   uint8_t* h_ws;
   int* h_argmax;
   float* h_max;
@@ -104,6 +106,8 @@ struct GemvArgs {
 constexpr int kHeadCounterBytes = 256;
 constexpr int kHeadStateBytes = 16;
 constexpr int kHeadMaxT = 16;
+constexpr int kHeadGroup = 8;       // clusters merged per group (first level)
+constexpr int kHeadMaxGroups = 32;  // groups the second level covers (256 clusters)
 
 // Shared-memory map of the barrier region (first 1 KiB).
 struct Bars {
@@ -970,51 +974,96 @@ __device__ __forceinline__ void head_merge_lanes(float& m, float& s, int& a, int
 }
 
 // End of a CTA's epilogue warp on the fused head: merge the four lanes of each
-// token, publish the warp's per-token states, and count the warp in; the
-// last of the clusters x kEpiWarps warps to arrive merges every state in
-// (cluster, warp) order and writes argmax, maximum and logsumexp.
+// token and publish the warp's per-token states; then a two-level merge, each
+// level done by the last warp to arrive and costing one round of loads:
+// the last warp of a group of kHeadGroup clusters merges the group's
+// 2 kHeadGroup states per token in (cluster, warp) order, and the last group
+// to finish merges the groups in order and writes argmax, maximum and
+// logsumexp.  Lanes 2t and 2t + 1 take token t, one half of the entries each.
+template <int NMAX>
+__device__ __forceinline__ void head_merge_entries(const uint8_t* base, int first, int count,
+                                                   int tok, float& m, float& s, int& am) {
+  float4 st[NMAX];
+#pragma unroll
+  for (int k = 0; k < NMAX; ++k)
+    st[k] = k < count ? __ldcg(reinterpret_cast<const float4*>(
+                            base + (static_cast<size_t>(first + k) * kHeadMaxT + tok) * kHeadStateBytes))
+                      : make_float4(-INFINITY, 0.f, __int_as_float(INT_MAX), 0.f);
+#pragma unroll
+  for (int k = 0; k < NMAX; ++k) head_merge(m, s, am, st[k].x, st[k].y, __float_as_int(st[k].z));
+}
+
 template <int SLOTS>
 __device__ void head_finish(const GemvArgs& a, const Work& wk, int ew, int lane,
                             float (&hm)[SLOTS], float (&hs)[SLOTS], int (&ha)[SLOTS]) {
   const int T = a.T;
-  const int entries = a.clusters * kEpiWarps;
-  const int me = (blockIdx.x / a.ksplit) * kEpiWarps + ew;
-  uint8_t* states = a.h_ws + kHeadCounterBytes;
+  const int cl = blockIdx.x / a.ksplit;
+  const int grp = cl / kHeadGroup;
+  const int ngroups = (a.clusters + kHeadGroup - 1) / kHeadGroup;
+  const int gcl0 = grp * kHeadGroup;                              // first cluster of the group
+  const int gcls = min(kHeadGroup, a.clusters - gcl0);           // clusters in the group
+  unsigned* counters = reinterpret_cast<unsigned*>(a.h_ws);
+  uint8_t* states = a.h_ws + kHeadCounterBytes;                  // (cluster, warp, token)
+  uint8_t* gstates = states + static_cast<size_t>(a.clusters) * kEpiWarps * kHeadMaxT * kHeadStateBytes;
 #pragma unroll
   for (int i = 0; i < SLOTS; ++i) {
     head_merge_lanes(hm[i], hs[i], ha[i], 1);
     head_merge_lanes(hm[i], hs[i], ha[i], 2);
     const int tok = (lane >> 2) + 8 * i;
     if ((lane & 3) == 0 && tok < T) {
-      float4 st = make_float4(hm[i], hs[i], __int_as_float(ha[i]), 0.f);
-      *reinterpret_cast<float4*>(states + (static_cast<size_t>(me) * kHeadMaxT + tok) * kHeadStateBytes) = st;
+      const int me = cl * kEpiWarps + ew;
+      *reinterpret_cast<float4*>(states + (static_cast<size_t>(me) * kHeadMaxT + tok) * kHeadStateBytes) =
+          make_float4(hm[i], hs[i], __int_as_float(ha[i]), 0.f);
     }
   }
   __threadfence();
   __syncwarp();
   unsigned last = 0;
   if (lane == 0)
-    last = atomicAdd(reinterpret_cast<unsigned*>(a.h_ws), 1u) == static_cast<unsigned>(entries - 1);
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return;
+    last = atomicAdd(counters + 1 + grp, 1u) == static_cast<unsigned>(gcls * kEpiWarps - 1);
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
   __threadfence();
-  for (int t = 0; t < T; ++t) {
+  // First level: this group's states.
+  const int tok = lane >> 1, half = lane & 1;
+  {
+    constexpr int kHalf = kHeadGroup * kEpiWarps / 2;
     float m = -INFINITY, s = 0.f;
     int am = INT_MAX;
-    for (int j = lane; j < entries; j += 32) {
-      const float4 st = __ldcg(reinterpret_cast<const float4*>(
-          states + (static_cast<size_t>(j) * kHeadMaxT + t) * kHeadStateBytes));
-      head_merge(m, s, am, st.x, st.y, __float_as_int(st.z));
+    if (tok < T) {
+      const int n = gcls * kEpiWarps;
+      const int first = half * kHalf;
+      head_merge_entries<kHalf>(states, gcl0 * kEpiWarps + first, max(0, min(kHalf, n - first)),
+                                tok, m, s, am);
     }
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) head_merge_lanes(m, s, am, d);
-    if (lane == 0) {
-      a.h_argmax[t] = am == INT_MAX ? -1 : am;
-      a.h_max[t] = m;
-      a.h_lse[t] = m + __logf(s);
-    }
+    head_merge_lanes(m, s, am, 1);
+    if (half == 0 && tok < T)
+      *reinterpret_cast<float4*>(gstates + (static_cast<size_t>(grp) * kHeadMaxT + tok) * kHeadStateBytes) =
+          make_float4(m, s, __int_as_float(am), 0.f);
+    if (lane == 0) *reinterpret_cast<volatile unsigned*>(counters + 1 + grp) = 0u;
   }
-  if (lane == 0) *reinterpret_cast<volatile unsigned*>(a.h_ws) = 0u;
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) last = atomicAdd(counters, 1u) == static_cast<unsigned>(ngroups - 1);
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  __threadfence();
+  // Second level: every group, in order.
+  {
+    constexpr int kHalf = kHeadMaxGroups / 2;
+    float m = -INFINITY, s = 0.f;
+    int am = INT_MAX;
+    if (tok < T) {
+      const int first = half * kHalf;
+      head_merge_entries<kHalf>(gstates, first, max(0, min(kHalf, ngroups - first)), tok, m, s,
+                                am);
+    }
+    head_merge_lanes(m, s, am, 1);
+    if (half == 0 && tok < T) {
+      a.h_argmax[tok] = am == INT_MAX ? -1 : am;
+      a.h_max[tok] = m;
+      a.h_lse[tok] = m + __logf(s);
+    }
+    if (lane == 0) *reinterpret_cast<volatile unsigned*>(counters) = 0u;
+  }
 }
 
 template <int SLOTS>

@@ -575,9 +575,11 @@ int nq_head_workspace_bytes(size_t* bytes) {
   if (!bytes) return NQ_EINVAL;
   DevInfo* d;
   if (int rc = dev_info(&d)) return rc;
-  // one state per (cluster, epilogue warp, token); clusters <= SMs
+  // one state per (cluster, epilogue warp, token) and per (group of
+  // kHeadGroup clusters, token); clusters <= SMs
+  const size_t groups = (static_cast<size_t>(d->sms) + kHeadGroup - 1) / kHeadGroup;
   *bytes = static_cast<size_t>(kHeadCounterBytes) +
-           static_cast<size_t>(d->sms) * kEpiWarps * kHeadMaxT * kHeadStateBytes;
+           (static_cast<size_t>(d->sms) * kEpiWarps + groups) * kHeadMaxT * kHeadStateBytes;
   return NQ_OK;
 }
 
@@ -588,6 +590,11 @@ int nq_gemv_head(const void* packed, const uint16_t* scales, const void* x_bf16,
   if (int rc = check_shape(K, N, bits)) return rc;
   if (T < 1 || T > kMaxT) return NQ_EINVAL;
   if (N > INT32_MAX) return NQ_EINVAL;  // row indices are int32
+  {
+    DevInfo* d;
+    if (int rc = dev_info(&d)) return rc;
+    if (d->sms > kHeadGroup * kHeadMaxGroups) return NQ_EUNSUPPORTED;  // merge covers 256 clusters
+  }
   if (!aligned16(packed) || !aligned16(scales) || !aligned16(x_bf16) || !aligned16(workspace) ||
       (y && !aligned16(y)))
     return NQ_EALIGN;
