@@ -162,6 +162,28 @@ int nq_gemv_head(const void* packed, const uint16_t* scales, const void* x_bf16,
 /* Bytes of workspace nq_gemv_head needs on the current device (any T, N). */
 int nq_head_workspace_bytes(size_t* bytes);
 
+/* nq_gemv_head for callers that cannot allocate device memory: a library
+ * plugged into a host runtime that owns every device allocation and hands it
+ * only the tensors it works on, or a latency-critical loop where a
+ * cudaMalloc / cudaFree (which synchronise the device) is not acceptable.
+ * No counterpart in the pages: it is an interface convenience, not part of
+ * the method.  Same arguments and results as nq_gemv_head, without the
+ * workspace: the scratch is one file-scope device array of
+ * NQ_HEAD_SCRATCH_BYTES, held by every GPU that loads the library until the
+ * process exits, enough for devices of up to 256 SMs (NQ_EUNSUPPORTED on a
+ * larger one).  The call allocates nothing.  The first call on a device looks
+ * up the array's device address (once per device, with that device current);
+ * make that first call before any stream capture.  Every call shares the
+ * array and finds the previous call's contents in it; the call clears the
+ * part that must start at zero (the arrival counter) on its stream before
+ * launching.  Calls that overlap on the GPU (other streams, other host
+ * threads without ordering) race on the array and give wrong results: order
+ * them on one stream. */
+#define NQ_HEAD_SCRATCH_BYTES 139520
+int nq_gemv_head_noalloc(const void* packed, const uint16_t* scales, const void* x_bf16, float* y,
+                         int64_t K, int64_t N, int T, int bits, int32_t* argmax, float* maxval,
+                         float* lse, nq_stream_t stream);
+
 /* Dequantised weights w[N, K] fp32 (device, row-major) = scale * code, exact.
  * Test aid: lets the decode path be checked bit for bit. */
 int nq_dequant(const void* packed, const uint16_t* scales, float* w, int64_t K, int64_t N,

@@ -20,7 +20,7 @@ import numpy as np
 __all__ = [
     "NQError", "ROUTE_AUTO", "ROUTE_MMA", "ROUTE_FFMA", "lib", "lib_path", "build",
     "packed_bytes", "pack", "unpack", "pack_device", "quantize_rtn", "gemv", "gemv_head",
-    "head_workspace_bytes", "dequant",
+    "head_workspace_bytes", "gemv_head_noalloc", "dequant",
     "last_device_error", "plan", "selftest_wait_timeout", "status_string", "layout_version",
     "QuantizedWeight", "EXPORTED",
 ]
@@ -47,6 +47,8 @@ _SIGS = {
     "nq_gemv_head": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp,
                             ctypes.c_size_t, _vp]),
     "nq_head_workspace_bytes": (_i32, [_szp]),
+    "nq_gemv_head_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp,
+                                    _vp]),
     "nq_dequant": (_i32, [_vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "nq_last_device_error": (_i32, [_vp]),
     "nq_gemv_plan": (_i32, [_i64, _i64, _i32, _i32, _i32, _i32, _ip, _ip, _ip, _ip, _ip]),
@@ -220,6 +222,26 @@ def gemv_head(packed, scales, x, K: int, N: int, T: int, bits: int, y=None, work
                               _dptr(argmax), _dptr(maxval), _dptr(lse), _dptr(workspace),
                               workspace.numel() * workspace.element_size(),
                               _stream_handle(stream)), "nq_gemv_head")
+    return argmax, maxval, lse
+
+
+def gemv_head_noalloc(packed, scales, x, K: int, N: int, T: int, bits: int, y=None,
+                      argmax=None, maxval=None, lse=None, stream=None):
+    """gemv_head through the entry point that allocates nothing: the library
+    uses its own fixed device scratch instead of a workspace.  Calls must not
+    overlap on the GPU.  Returns (argmax, maxval, lse); output tensors the
+    caller does not pass are created here (torch memory)."""
+    import torch
+    dev = x.device
+    if argmax is None:
+        argmax = torch.empty(T, dtype=torch.int32, device=dev)
+    if maxval is None:
+        maxval = torch.empty(T, dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty(T, dtype=torch.float32, device=dev)
+    _check(lib().nq_gemv_head_noalloc(_dptr(packed), _dptr(scales), _dptr(x), _dptr(y), K, N, T,
+                                      bits, _dptr(argmax), _dptr(maxval), _dptr(lse),
+                                      _stream_handle(stream)), "nq_gemv_head_noalloc")
     return argmax, maxval, lse
 
 

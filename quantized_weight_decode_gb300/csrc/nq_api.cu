@@ -618,6 +618,44 @@ int nq_gemv_head(const void* packed, const uint16_t* scales, const void* x_bf16,
   return launch_plan(p, packed, scales, x_bf16, y, K, N, T, st, h);
 }
 
+// ---------------------------------------------------------------- fused head, no allocation
+// The scratch of nq_gemv_head_noalloc: one file-scope device array, present on
+// every GPU that loads the library until the process exits.  Host code only
+// sees a stand-in for it; the device address comes from cudaGetSymbolAddress,
+// taken once per device with that device current.
+static_assert(NQ_HEAD_SCRATCH_BYTES ==
+                  kHeadCounterBytes + (256 * kEpiWarps + 256 / kHeadGroup) * kHeadMaxT * kHeadStateBytes,
+              "the no-allocation scratch covers devices of up to 256 SMs");
+static __device__ __align__(256) unsigned char g_head_scratch[NQ_HEAD_SCRATCH_BYTES];
+void* g_head_scratch_addr[kMaxDevices] = {};
+
+int nq_gemv_head_noalloc(const void* packed, const uint16_t* scales, const void* x_bf16, float* y,
+                         int64_t K, int64_t N, int T, int bits, int32_t* argmax, float* maxval,
+                         float* lse, nq_stream_t stream) {
+  size_t need = 0;
+  if (int rc = nq_head_workspace_bytes(&need)) return rc;
+  if (need > NQ_HEAD_SCRATCH_BYTES) return NQ_EUNSUPPORTED;  // more SMs than the scratch covers
+  int dev;
+  if (int rc = current_device(&dev)) return rc;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_head_scratch_addr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_head_scratch) != cudaSuccess || !p) {
+        (void)cudaGetLastError();
+        return NQ_ECUDA;
+      }
+      g_head_scratch_addr[dev] = p;
+    }
+    ws = g_head_scratch_addr[dev];
+  }
+  // nq_gemv_head clears the arrival counter (the part that must start at
+  // zero) on the stream before its launch.
+  return nq_gemv_head(packed, scales, x_bf16, y, K, N, T, bits, argmax, maxval, lse, ws,
+                      NQ_HEAD_SCRATCH_BYTES, stream);
+}
+
 int nq_gemv_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, int* route_out,
                  int* ksplit_out, int* clusters_out, int* stages_out, int* smem_out) {
   Plan p;
