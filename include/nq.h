@@ -125,6 +125,26 @@ int nq_pack_device(const int8_t* codes, const uint16_t* scales, int64_t K, int64
 int nq_quantize_rtn(const float* w, int64_t K, int64_t N, int bits,
                     int8_t* codes_out, uint16_t* scales_out, nq_stream_t stream);
 
+/* Device searched encoder (the "grouped_search" encoder of the page named
+ * above): per 64-group, the FP16 scale is the best of 50 candidates by
+ * importance-weighted squared error sum_k q_k (w_k - s c_k)^2, q the
+ * per-channel importance (an imatrix, mean squared input activation).  The
+ * page does not list the candidates; this library's: with a = max|w| and
+ * qmax = 7 / 15 / 31, h_i = FP16 round-to-nearest-even of
+ * 12 a / (12 (qmax + 1) - i), i = 0..24 (a / L for L from qmax + 1 down to
+ * qmax - 1), each tried as +h_i and -h_i (negative scales let the group's
+ * largest weight use code -2^(bits-1)).  Codes are round-half-even(w / s)
+ * clamped to the range; the error is accumulated in fp64 over the group in
+ * order; ties go to the lower candidate (+h_0, -h_0, +h_1, ...).  i = 12 is
+ * the round-to-nearest scale, so the result is never worse than
+ * nq_quantize_rtn under the same importance.
+ * w: device fp32 [N, K]; imatrix: device fp32 [K] (>= 0), or NULL for all
+ * ones; codes_out: device int8 [N, K]; scales_out: device FP16 bits [N, K/64]
+ * (same outputs as nq_quantize_rtn).  A group whose every candidate overflows
+ * FP16 sets NQ_ERANGE in the device status word. */
+int nq_quantize_search(const float* w, const float* imatrix, int64_t K, int64_t N, int bits,
+                       int8_t* codes_out, uint16_t* scales_out, nq_stream_t stream);
+
 /* y[T, N] (fp32, device, row-major, overwritten) = x[T, K] (bf16 bit
  * patterns, device, row-major) times dequant(W)^T, W given by its packed codes
  * and packed scales (device, layout above).  1 <= T <= 16.

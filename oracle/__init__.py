@@ -151,6 +151,85 @@ def rtn_encode(w: np.ndarray, bits: int, chunk_rows: int = 2048):
 
 
 # --------------------------------------------------------------------------
+# Searched encoder ("grouped_search" on the 3090 model card, section "What is
+# different from the upstream artifact"): each group's FP16 scale is the best
+# of 50 candidates by importance-weighted squared error, importance being a
+# per-channel imatrix (mean squared input activation); scales may be negative.
+# The page does not list the candidates; the reading taken here (also in the
+# design notes): with a = max|w| over the group and qmax the largest positive
+# code, the 25 magnitudes h_i = fp16_rne(12 a / (12 (qmax + 1) - i)), i = 0..24,
+# i.e. a / L for L from qmax + 1 down to qmax - 1 in steps of 1/12, each tried
+# as +h_i and -h_i (candidate 2i and 2i + 1).  A candidate's codes are
+# clamp(rint(w / s)) as in the round-to-nearest encoder (a zero scale gives
+# code 0); its error is sum_k q_k (w_k - s c_k)^2, accumulated over k in
+# order in fp64 with every product and sum rounded separately.  The smallest
+# error wins, ties to the lower candidate number; candidates whose scale
+# overflows FP16 take no part.  i = 12 is the round-to-nearest scale, so the
+# search never does worse than that encoder under the same importance.
+# --------------------------------------------------------------------------
+SEARCH_STEPS = 25
+
+
+def search_candidates(a: np.ndarray, qmax: int) -> np.ndarray:
+    """FP16 bit patterns of the 50 candidate scales for group maxima a (fp64),
+    shape a.shape + (50,), in candidate order (+h_0, -h_0, +h_1, ...)."""
+    a = np.asarray(a, dtype=np.float64)
+    den = 12.0 * (qmax + 1) - np.arange(SEARCH_STEPS, dtype=np.float64)
+    h = f64_to_fp16_bits((12.0 * a)[..., None] / den)          # [..., 25]
+    out = np.empty(a.shape + (2 * SEARCH_STEPS,), dtype=np.uint16)
+    out[..., 0::2] = h
+    out[..., 1::2] = h | np.uint16(0x8000)
+    return out
+
+
+def search_encode(w: np.ndarray, bits: int, imatrix=None, chunk_groups: int = 2048):
+    """Searched encode: returns (codes int8 [N, K], scale bits uint16 [N, K/64]).
+    imatrix: per-channel importance [K] (>= 0), None for all ones.  Raises
+    ValueError if every candidate of some group overflows FP16."""
+    w = np.asarray(w, dtype=np.float32)
+    n, k = w.shape
+    if k % GROUP:
+        raise ValueError("K must be a multiple of 64")
+    g = k // GROUP
+    lo, hi = code_range(bits)
+    q = np.ones(k, np.float64) if imatrix is None else np.asarray(imatrix, np.float32).astype(np.float64)
+    qg = q.reshape(g, GROUP)
+    wg = w.reshape(n * g, GROUP).astype(np.float64)
+    qrow = np.tile(qg, (n, 1))                                   # [n*g, 64]
+    codes = np.empty((n * g, GROUP), np.int8)
+    scales = np.empty(n * g, np.uint16)
+    for r0 in range(0, n * g, chunk_groups):
+        r1 = min(n * g, r0 + chunk_groups)
+        ww, qq = wg[r0:r1], qrow[r0:r1]
+        cand = search_candidates(np.abs(ww).max(axis=1), QMAX[bits])      # [m, 50]
+        sv = fp16_to_f64(cand)[:, :, None]                                 # [m, 50, 1]
+        with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+            c = np.rint(ww[:, None, :] / sv)
+            c = np.where(sv == 0.0, 0.0, c)
+            c = np.clip(c, lo, hi)
+            d = ww[:, None, :] - sv * c          # (overflowed candidates give NaN here)
+            err = np.add.accumulate(qq[:, None, :] * (d * d), axis=2)[:, :, -1]   # in order over k
+        err = np.where(np.isinf(sv[:, :, 0]), np.inf, err)
+        if np.any(np.all(np.isinf(sv[:, :, 0]), axis=1)):
+            raise ValueError("every candidate scale overflows FP16")
+        best = np.argmin(err, axis=1)                                      # first minimum
+        idx = np.arange(r1 - r0)
+        scales[r0:r1] = cand[idx, best]
+        codes[r0:r1] = c[idx, best].astype(np.int8)
+    return codes.reshape(n, k), scales.reshape(n, g)
+
+
+def weighted_error(w: np.ndarray, codes: np.ndarray, scale_bits: np.ndarray, imatrix=None):
+    """sum_k q_k (w_k - s c_k)^2 per group [N, K/64] in fp64 (for tests)."""
+    w = np.asarray(w, dtype=np.float32).astype(np.float64)
+    n, k = w.shape
+    q = np.ones(k) if imatrix is None else np.asarray(imatrix, np.float32).astype(np.float64)
+    s = np.repeat(fp16_to_f64(scale_bits), GROUP, axis=1)
+    d = w - s * codes.astype(np.float64)
+    return (q[None, :] * d * d).reshape(n, k // GROUP, GROUP).sum(axis=2)
+
+
+# --------------------------------------------------------------------------
 # Dequantisation and the product.
 # Pin: exhaustive FP16 x code sweep (product exact in fp32), one-hot and
 # constant inputs, and exact rational arithmetic on small shapes.

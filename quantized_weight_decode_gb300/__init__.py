@@ -19,7 +19,7 @@ import numpy as np
 
 __all__ = [
     "NQError", "ROUTE_AUTO", "ROUTE_MMA", "ROUTE_FFMA", "lib", "lib_path", "build",
-    "packed_bytes", "pack", "unpack", "pack_device", "quantize_rtn", "gemv", "gemv_head",
+    "packed_bytes", "pack", "unpack", "pack_device", "quantize_rtn", "quantize_search", "gemv", "gemv_head",
     "head_workspace_bytes", "gemv_head_noalloc", "dequant",
     "last_device_error", "plan", "selftest_wait_timeout", "status_string", "layout_version",
     "QuantizedWeight", "EXPORTED",
@@ -42,6 +42,7 @@ _SIGS = {
     "nq_unpack": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _vp]),
     "nq_pack_device": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp]),
     "nq_quantize_rtn": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _vp]),
+    "nq_quantize_search": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp]),
     "nq_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "nq_gemv_ex": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp]),
     "nq_gemv_head": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp,
@@ -180,6 +181,20 @@ def quantize_rtn(w, bits: int, codes=None, scales=None, stream=None):
         scales = torch.empty((N, K // 64), dtype=torch.int16, device=w.device)
     _check(lib().nq_quantize_rtn(_dptr(w), K, N, bits, _dptr(codes), _dptr(scales),
                                  _stream_handle(stream)), "nq_quantize_rtn")
+    return codes, scales
+
+
+def quantize_search(w, bits: int, imatrix=None, codes=None, scales=None, stream=None):
+    """Searched encoder on the device: w fp32 [N, K] (device tensor), imatrix
+    fp32 [K] or None -> (codes int8 [N, K], scales int16 FP16 bits [N, K/64])."""
+    import torch
+    N, K = w.shape
+    if codes is None:
+        codes = torch.empty((N, K), dtype=torch.int8, device=w.device)
+    if scales is None:
+        scales = torch.empty((N, K // 64), dtype=torch.int16, device=w.device)
+    _check(lib().nq_quantize_search(_dptr(w), _dptr(imatrix), K, N, bits, _dptr(codes),
+                                    _dptr(scales), _stream_handle(stream)), "nq_quantize_search")
     return codes, scales
 
 

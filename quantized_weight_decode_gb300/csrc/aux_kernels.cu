@@ -4,6 +4,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <climits>
+#include <cmath>
 #include <cstdint>
 
 #include "gemv.cuh"
@@ -170,6 +172,108 @@ cudaError_t launch_quantize_rtn(const float* w, long long K, long long N, int bi
   const int block = 256;  // 8 groups per block
   const long long grid = (ngroups * 32 + block - 1) / block;
   quantize_rtn_kernel<<<grid, block, 0, st>>>(w, K, ngroups, G, bits, codes, scales, status);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ searched encoder
+// The "grouped_search" encoder of the page "Qwen3.8-27B for NInfer on the RTX
+// 3090" (section "What is different from the upstream artifact"): each
+// group's FP16 scale is the best of 50 candidates by importance-weighted
+// squared error, importance q_k per channel (an imatrix); scales may be
+// negative.  Candidates (the page gives none; our reading): with a = max|w|,
+// h_i = fp16_rne(12 a / (12 (qmax + 1) - i)), i = 0..24, tried as +h_i
+// (candidate 2i) and -h_i (2i + 1); codes clamp(rint(w / s)) (0 for a zero
+// scale); error sum_k q_k (w_k - s c_k)^2 accumulated over k in order in fp64,
+// every product and sum rounded on its own (no fused multiply-add), so the
+// choice is reproducible bit for bit.  Smallest error wins, ties to the lower
+// candidate; candidates whose scale overflows FP16 take no part (if all do,
+// NQ_ERANGE).  One warp per group: lane l holds weights 2l, 2l + 1 and
+// candidates l and l + 32.
+__global__ void quantize_search_kernel(const float* __restrict__ w, const float* __restrict__ imp,
+                                       long long K, long long ngroups, int G, int bits,
+                                       int8_t* __restrict__ codes, uint16_t* __restrict__ scales,
+                                       int* status) {
+  const long long gw = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= ngroups) return;
+  const long long n = gw / G;
+  const int g = static_cast<int>(gw - n * G);
+  const long long off = n * K + static_cast<long long>(g) * kGroup + 2 * lane;
+  const float2 v = *reinterpret_cast<const float2*>(w + off);
+  const float2 qv = imp ? *reinterpret_cast<const float2*>(imp + static_cast<long long>(g) * kGroup + 2 * lane)
+                        : make_float2(1.f, 1.f);
+  float a = fmaxf(fabsf(v.x), fabsf(v.y));
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
+  const int qmax = (1 << (bits - 1)) - 1;
+  const double lo = -static_cast<double>(qmax) - 1.0, hi = static_cast<double>(qmax);
+  auto cand_bits = [&](int j) -> uint16_t {
+    const int i = j >> 1;
+    const __half h = __double2half((12.0 * static_cast<double>(a)) / (12.0 * (qmax + 1) - i));
+    return static_cast<uint16_t>(__half_as_ushort(h) | ((j & 1) << 15));
+  };
+  auto code_of = [&](double x, double s) -> double {
+    return s == 0.0 ? 0.0 : fmin(fmax(rint(x / s), lo), hi);
+  };
+  double sj[2], err[2] = {0.0, 0.0};
+  bool valid[2];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int j = lane + 32 * c;
+    const uint16_t b = j < 50 ? cand_bits(j) : 0x7C00u;
+    valid[c] = j < 50 && (b & 0x7C00u) != 0x7C00u;
+    sj[c] = valid[c] ? static_cast<double>(__half2float(__ushort_as_half(b))) : 0.0;
+  }
+  for (int k = 0; k < kGroup; ++k) {
+    const double wk = __shfl_sync(0xffffffffu, (k & 1) ? v.y : v.x, k >> 1);
+    const double qk = __shfl_sync(0xffffffffu, (k & 1) ? qv.y : qv.x, k >> 1);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const double d = __dsub_rn(wk, __dmul_rn(sj[c], code_of(wk, sj[c])));
+      err[c] = __dadd_rn(err[c], __dmul_rn(qk, __dmul_rn(d, d)));
+    }
+  }
+  double be = INFINITY;
+  int bj = INT_MAX;
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+    if (valid[c] && err[c] < be) {
+      be = err[c];
+      bj = lane + 32 * c;
+    }
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    const double oe = __shfl_xor_sync(0xffffffffu, be, m);
+    const int oj = __shfl_xor_sync(0xffffffffu, bj, m);
+    if (oe < be || (oe == be && oj < bj)) {
+      be = oe;
+      bj = oj;
+    }
+  }
+  uint16_t sbits = 0x7C00u;
+  double s = 0.0;
+  if (bj == INT_MAX) {
+    if (lane == 0) atomicCAS(status, 0, -3);
+  } else {
+    sbits = cand_bits(bj);
+    s = static_cast<double>(__half2float(__ushort_as_half(sbits)));
+  }
+  char2 cc;
+  cc.x = static_cast<signed char>(code_of(v.x, s));
+  cc.y = static_cast<signed char>(code_of(v.y, s));
+  *reinterpret_cast<char2*>(codes + off) = cc;
+  if (lane == 0) scales[n * G + g] = sbits;
+}
+
+cudaError_t launch_quantize_search(const float* w, const float* imatrix, long long K, long long N,
+                                   int bits, int8_t* codes, uint16_t* scales, int* status,
+                                   cudaStream_t st) {
+  const int G = static_cast<int>(K / kGroup);
+  const long long ngroups = N * G;
+  const int block = 256;  // 8 groups per block
+  const long long grid = (ngroups * 32 + block - 1) / block;
+  quantize_search_kernel<<<grid, block, 0, st>>>(w, imatrix, K, ngroups, G, bits, codes, scales,
+                                                 status);
   return cudaGetLastError();
 }
 

@@ -26,6 +26,8 @@ cudaError_t launch_dequant(const void*, const uint16_t*, float*, long long, long
                            cudaStream_t);
 cudaError_t launch_quantize_rtn(const float*, long long, long long, int, int8_t*, uint16_t*, int*,
                                 cudaStream_t);
+cudaError_t launch_quantize_search(const float*, const float*, long long, long long, int, int8_t*,
+                                   uint16_t*, int*, cudaStream_t);
 cudaError_t launch_selftest_timeout(unsigned long long, int*, cudaStream_t);
 int* device_status_ptr();
 
@@ -548,6 +550,21 @@ int nq_quantize_rtn(const float* w, int64_t K, int64_t N, int bits, int8_t* code
   if (int rc = dev_info(&d)) return rc;
   if (launch_quantize_rtn(w, K, N, bits, codes_out, scales_out, d->status,
                           reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return NQ_ECUDA;
+  }
+  return NQ_OK;
+}
+
+int nq_quantize_search(const float* w, const float* imatrix, int64_t K, int64_t N, int bits,
+                       int8_t* codes_out, uint16_t* scales_out, nq_stream_t stream) {
+  if (int rc = check_shape(K, N, bits)) return rc;
+  if (!w || !codes_out || !scales_out) return NQ_EINVAL;
+  if (!aligned16(w) || !aligned16(codes_out) || (imatrix && !aligned16(imatrix))) return NQ_EALIGN;
+  DevInfo* d;
+  if (int rc = dev_info(&d)) return rc;
+  if (launch_quantize_search(w, imatrix, K, N, bits, codes_out, scales_out, d->status,
+                             reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
     (void)cudaGetLastError();
     return NQ_ECUDA;
   }

@@ -91,3 +91,16 @@ def torch_generator(seed: int, device):
     g = torch.Generator(device=device)
     g.manual_seed(int(seed))
     return g
+
+
+def imatrix(rng: np.random.Generator, k: int, tokens: int = 64, outlier_frac: float = 0.01,
+            outlier_mult: float = 20.0) -> np.ndarray:
+    """A synthetic importance matrix: per channel, the mean squared value of
+    `tokens` activation draws N(0, 1) with a fraction of outlier channels
+    scaled by `outlier_mult` (fp32 [k]).  Stands in for an imatrix gathered
+    from calibration text."""
+    x = rng.standard_normal((tokens, k), dtype=np.float32)
+    n_out = int(round(outlier_frac * k))
+    if n_out:
+        x[:, rng.choice(k, n_out, replace=False)] *= np.float32(outlier_mult)
+    return np.mean(x.astype(np.float64) ** 2, axis=0).astype(np.float32)

@@ -311,3 +311,92 @@ def test_head_rows_are_independent_tokens():
     am2, _, lse2 = oracle.head_reduce(y + 123.5)
     assert np.array_equal(am, am2)
     assert np.all(np.abs(lse2 - (lse + 123.5)) <= 1e-12 * np.abs(lse2))
+
+
+# ---------------------------------------------------------------- searched encoder
+def _exact_group(values, step_bits):
+    """One 64-weight row group w = step * values (values integers), step an FP16
+    bit pattern; returns fp32 [1, 64]."""
+    step = float(oracle.fp16_to_f64(np.array([step_bits], np.uint16))[0])
+    return (np.asarray(values, np.float64) * step).astype(np.float32)[None, :]
+
+
+def test_search_never_worse_than_rtn():
+    rng = synth.generator(0, 900)
+    for bits in (4, 5, 6):
+        w = synth.gauss_weights(rng, 24, 512)
+        w[3, 64:128] *= np.float32(50.0)          # a group with one large channel
+        q = synth.imatrix(rng, 512)
+        for imp in (None, q):
+            c, s = oracle.search_encode(w, bits, imp)
+            cr, sr = oracle.rtn_encode(w, bits)
+            e = oracle.weighted_error(w, c, s, imp)
+            er = oracle.weighted_error(w, cr, sr, imp)
+            assert np.all(e <= er * (1 + 1e-12)), bits
+            lo, hi = oracle.code_range(bits)
+            assert c.min() >= lo and c.max() <= hi
+
+
+def test_search_picks_a_negative_scale_when_only_it_is_exact():
+    # values -7..8: representable as step * c with c in [-8, 7] only if the
+    # scale is -step (the +8 needs code -8); the largest value is 8 steps, so
+    # the first candidate magnitude h_0 = fp16(a / 8) is the step itself.
+    vals = (np.arange(64) % 16) - 7                        # -7 .. 8
+    w = _exact_group(vals, 0x2000)                           # step 2^-7
+    c, s = oracle.search_encode(w, 4)
+    assert s[0, 0] == 0xA000                                 # -2^-7: candidate 1
+    assert np.array_equal(c[0], -vals)
+    assert oracle.weighted_error(w, c, s)[0, 0] == 0.0
+    # -8 .. 7: the positive candidate 0 is exact
+    vals = (np.arange(64) % 16) - 8
+    w = _exact_group(vals, 0x2000)
+    c, s = oracle.search_encode(w, 4)
+    assert s[0, 0] == 0x2000 and np.array_equal(c[0], vals)
+
+
+def test_search_ties_go_to_the_first_candidate():
+    rng = synth.generator(0, 901)
+    w = synth.gauss_weights(rng, 2, 64)
+    c, s = oracle.search_encode(w, 5, imatrix=np.zeros(64, np.float32))   # every error 0
+    cand = oracle.search_candidates(np.abs(w.astype(np.float64)).max(axis=1), 15)
+    assert np.array_equal(s[:, 0], cand[:, 0])
+    z = np.zeros((1, 128), np.float32)
+    c, s = oracle.search_encode(z, 6)
+    assert np.all(s == 0) and np.all(c == 0)
+
+
+def test_search_single_important_channel_matches_exact_brute_force():
+    """Importance on one channel only: the chosen candidate must minimise that
+    one weight's error, checked in exact rational arithmetic over the 50
+    candidates (first one on ties)."""
+    rng = synth.generator(0, 902)
+    for bits in (4, 5, 6):
+        lo, hi = oracle.code_range(bits)
+        for trial in range(6):
+            w = synth.gauss_weights(rng, 1, 64)
+            j = int(rng.integers(64))
+            q = np.zeros(64, np.float32)
+            q[j] = 1.0
+            c, s = oracle.search_encode(w, bits, q)
+            cand = oracle.search_candidates(np.array([np.abs(w.astype(np.float64)).max()]),
+                                            oracle.QMAX[bits])[0]
+            wj = Fraction(float(w[0, j]))
+            errs = []
+            for b in cand:
+                sv = Fraction(float(oracle.fp16_to_f64(np.array([b], np.uint16))[0]))
+                code = 0 if sv == 0 else min(max(round(wj / sv), lo), hi)   # round: half to even
+                errs.append((wj - sv * code) ** 2)
+            best = min(range(len(errs)), key=lambda i: (errs[i], i))
+            assert s[0, 0] == cand[best], (bits, trial)
+
+
+def test_search_importance_scale_invariance_and_overflow():
+    rng = synth.generator(0, 903)
+    w = synth.gauss_weights(rng, 8, 256)
+    q = synth.imatrix(rng, 256)
+    c1, s1 = oracle.search_encode(w, 4, q)
+    c2, s2 = oracle.search_encode(w, 4, q * np.float32(4.0))     # errors scale exactly by 4
+    assert np.array_equal(c1, c2) and np.array_equal(s1, s2)
+    big = np.full((1, 64), 7.0e5, np.float32)                     # every candidate > 65504
+    with pytest.raises(ValueError):
+        oracle.search_encode(big, 4)
