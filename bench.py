@@ -305,6 +305,48 @@ def fused_head_times(torch, nqp, entries, stream, reps):
     return out
 
 
+def encoder_times(torch, nqp, dev, reps=3):
+    """Device round-to-nearest and searched encoders on one gate+up-sized
+    fp32 matrix (K=5120, N=34816, 4-bit, synthetic imatrix), CUDA events; and
+    the CPU oracle's searched encoder on a bounded sample of its groups."""
+    import oracle
+    import synth
+    K, N, bits = HIDDEN, 2 * INTER, 4
+    g = torch.Generator(device=dev)
+    g.manual_seed(4242)
+    w = torch.randn((N, K), generator=g, device=dev, dtype=torch.float32).mul_(0.02)
+    imp = torch.from_numpy(synth.imatrix(synth.generator(4242, 1), K)).to(dev)
+    codes = torch.empty((N, K), dtype=torch.int8, device=dev)
+    scales = torch.empty((N, K // 64), dtype=torch.int16, device=dev)
+    groups = N * K // 64
+    out = {"shape": {"K": K, "N": N, "bits": bits, "groups": groups}}
+    for name, fn in (("rtn", lambda: nqp.quantize_rtn(w, bits, codes=codes, scales=scales)),
+                     ("search", lambda: nqp.quantize_search(w, bits, imp, codes=codes, scales=scales))):
+        fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        out[name] = {"ms": round(ms, 3), "mgroups_per_s": round(groups / ms / 1e3, 1)}
+    rc = nqp.last_device_error()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} in the encoders")
+    rows = 64                                   # bounded CPU sample: 64 rows = 5120 groups
+    ws = w[:rows].cpu().numpy()
+    t0 = time.perf_counter()
+    oracle.search_encode(ws, bits, imp.cpu().numpy())
+    el = time.perf_counter() - t0
+    out["search_oracle_cpu"] = {"mgroups_per_s": round(rows * K / 64 / el / 1e6, 4), "cores": 1,
+                                "sample": f"{rows} rows x {K} (fp64 numpy, one thread)"}
+    del w, codes, scales
+    return out
+
+
 def capture(torch, nqp, entries, ys, T, kind, stream):
     sel = [e for e in entries if e["kind"] == kind]
 
@@ -398,6 +440,9 @@ def run_ours(args, rank, world, local_rank):
     # ---------------- fused verify head (argmax, maximum, logsumexp per token)
     head_fused = fused_head_times(torch, nqp, entries, stream, reps=max(10, min(args.steps, 50)))
 
+    # ---------------- offline encoders on one gate+up-sized matrix
+    encoders = encoder_times(torch, nqp, dev) if rank == 0 else None
+
     # ---------------- end to end: x from pinned host, logits back to pinned host
     x_host = torch.empty(x_arena.shape, dtype=x_arena.dtype, pin_memory=True)
     x_host.copy_(x_arena)
@@ -464,6 +509,7 @@ def run_ours(args, rank, world, local_rank):
         "per_T": per_t,
         "kernels": kernels,
         "head_fused": head_fused,
+        "encoders": encoders,
         "plans": {f"{k}_T{T}": nqp.plan(e["K"], e["N"], T, e["bits"])
                   for T in TS for k in kinds
                   for e in [next(x for x in entries if x["kind"] == k)]},

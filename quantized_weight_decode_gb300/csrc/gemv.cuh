@@ -772,7 +772,7 @@ __device__ void consumer_xreg(const GemvArgs& a, uint8_t* smem, const Bars& bars
 
   uint32_t xr[GWM][NT][8];
   float inv[NT][2];
-  if constexpr (BITS == 4) {
+  if constexpr (BITS == 4 && NT == 1) {   // (the planner takes it for T <= 2 only)
     if (a.off_xh >= 0) {
       const bool f16 = stage_x_f16(a, smem, wk, warp, lane);
       if (f16) {

@@ -162,7 +162,8 @@ bool layout_for(const Plan& base, int G, int T, int bits, int ks, int sg, int mi
   // with T; from T = 4 on they exceed what the shorter decode saves.)
   p.off_xh = -1;
   p.xh_stage0 = p.stages;
-  if (x_in_regs && bits == 4 && T <= kF16MaxT && env_int("NQ_X_F16", 1) != 0) {
+  if (x_in_regs && p.ntok == kNtokXreg && bits == 4 && T <= kF16MaxT &&
+      env_int("NQ_X_F16", 1) != 0) {
     const int xh_bytes = align_up(gc_max * T * 128, 128);
     const int off = (p.smem - xh_bytes) / 128 * 128;
     if (off >= p.off_ring + p.stage_bytes) {
