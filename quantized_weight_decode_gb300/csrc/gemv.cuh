@@ -70,6 +70,15 @@ constexpr int kXregMaxGroups = 5;  // (the slice-length dispatch covers 1..5)
 // kXreg2MaxGroups groups per warp slice.
 constexpr int kNtokXreg2 = 4;
 constexpr int kXreg2MaxGroups = 3;
+// Row tiles per hand-off: the x-in-register consumers with one token block
+// (T <= 8) take the tiles of their cluster in pairs (two ring stages, two
+// accumulator sets, one partial buffer), which halves the per-job bookkeeping
+// of consumers and epilogue; the other variants hand over one tile at a time
+// (with two token blocks a second accumulator set costs more registers and
+// buffer space than it saves).  (Route 1 is the MMA route; the FMA route's
+// NTOK is its token count.)
+template <int ROUTE, int NTOK>
+constexpr int kJobTiles = (ROUTE == 1 && NTOK == kNtokXreg) ? 2 : 1;
 
 enum Route : int { kRouteMma = 1, kRouteFfma = 2 };
 
@@ -567,6 +576,37 @@ __device__ __forceinline__ bool hand_partial_mma(const GemvArgs& a, uint8_t* sme
   return true;
 }
 
+// Hand over the partials of JT consecutive tiles (tile jt at offset jt 16 T
+// of the slot); tiles past the cluster's last are zero.
+template <int NT, int JT>
+__device__ __forceinline__ bool hand_partials_mma(const GemvArgs& a, uint8_t* smem,
+                                                  const Bars& bars, const Waiter& wt, int warp,
+                                                  int lane, int b, uint32_t nuse,
+                                                  const float (&acc)[JT][NT][4]) {
+  const int q = lane >> 2, r = lane & 3;
+  const int T = a.T;
+  if (!wt.wait_warp<false>(bars.red_empty(b), (nuse & 1u) ^ 1u)) return false;
+  float* slot = reinterpret_cast<float*>(smem + a.off_red) + (b * kWarps + warp) * JT * 16 * T;
+#pragma unroll
+  for (int jt = 0; jt < JT; ++jt) {
+    float* st = slot + jt * 16 * T;
+#pragma unroll
+    for (int nb = 0; nb < NT; ++nb) {
+      const int t0 = 8 * nb + 2 * r;
+      if (t0 < T) {
+        st[t0 * 16 + q] = acc[jt][nb][0];
+        st[t0 * 16 + q + 8] = acc[jt][nb][2];
+      }
+      if (t0 + 1 < T) {
+        st[(t0 + 1) * 16 + q] = acc[jt][nb][1];
+        st[(t0 + 1) * 16 + q + 8] = acc[jt][nb][3];
+      }
+    }
+  }
+  mbar_arrive(bars.red_full(b));  // every lane: count = 32 per warp
+  return true;
+}
+
 // NG consecutive groups of a warp slice, unrolled without branches.
 template <int BITS, int NT, int GWM, int NG, bool F16>
 __device__ __forceinline__ void slice_xr(const uint8_t* codes, const uint8_t* scales,
@@ -698,18 +738,18 @@ __device__ inline bool stage_x_f16(const GemvArgs& a, uint8_t* smem, const Work&
   return stat[32] == 0u;
 }
 
-// The job loop of the x-in-registers consumer: per job, wait for the stage,
-// run the warp's slice (n groups, one straight-line body per slice length,
-// so the compiler can overlap one group's decode with the previous group's
-// MMAs), release the stage, hand the partial over.  F16: fp16 route; the
-// partial is brought back to the scale of x (inv) and rows q + 8 divided by
-// 16 before it is handed over.
-template <int BITS, int GWM, int NT, bool F16>
-__device__ __forceinline__ void xreg_jobs(const GemvArgs& a, uint8_t* smem, const Bars& bars,
-                                          const Waiter& wt, const Work& wk, int warp, int lane,
-                                          int n, int codes_off, int scales_off,
-                                          const uint32_t (&xr)[GWM][NT][8],
-                                          const float (&inv)[NT][2]) {
+// The job loop of the x-in-registers consumer, for a slice of NG groups (one
+// straight-line body, so the compiler can overlap one group's decode with the
+// previous group's MMAs): per pair of row tiles (one tile with two token
+// blocks), wait for each tile's stage, run the slice, release the stage; then
+// hand the partials over at once.
+// F16: fp16 route; the partials are brought back to the scale of x (inv) and
+// rows q + 8 divided by 16 before they are handed over.
+template <int BITS, int GWM, int NT, bool F16, int NG>
+__device__ void xreg_jobs(const GemvArgs& a, uint8_t* smem, const Bars& bars, const Waiter& wt,
+                          const Work& wk, int warp, int lane, int codes_off, int scales_off,
+                          const uint32_t (&xr)[GWM][NT][8], const float (&inv)[NT][2]) {
+  constexpr int JT = NT == 1 ? 2 : 1;   // = kJobTiles of the kernel
   const int q = lane >> 2;
   const uint8_t* ring = smem + a.off_ring;
   float inv16[NT][2];
@@ -720,40 +760,68 @@ __device__ __forceinline__ void xreg_jobs(const GemvArgs& a, uint8_t* smem, cons
   }
   int stage = 0;
   uint32_t phase = 0;
-  int rb = 0;        // partial buffer of this job
+  int rb = 0;        // partial buffer of this pair
   uint32_t rn = 0;   // uses of that buffer so far
-  for (int j = 0; j < wk.njobs; ++j) {
-    float acc[NT][4];
+  for (int j = 0; j < wk.njobs; j += JT) {
+    float acc[JT][NT][4];
 #pragma unroll
-    for (int nb = 0; nb < NT; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
-    if (!wt.wait_warp<false>(bars.full(stage), phase)) return;
-    const uint8_t* st = ring + stage * a.stage_bytes;
-    const uint8_t* cs = st + codes_off;
-    const uint8_t* ss = st + scales_off;
-    switch (n) {
-      case 1: slice_xr<BITS, NT, GWM, 1, F16>(cs, ss, xr, lane, q, acc); break;
-      case 2: slice_xr<BITS, NT, GWM, 2, F16>(cs, ss, xr, lane, q, acc); break;
-      case 3: slice_xr<BITS, NT, GWM, 3, F16>(cs, ss, xr, lane, q, acc); break;
-      case 4: slice_xr<BITS, NT, GWM, 4, F16>(cs, ss, xr, lane, q, acc); break;
-      case 5: slice_xr<BITS, NT, GWM, 5, F16>(cs, ss, xr, lane, q, acc); break;
-      default: break;
+    for (int jt = 0; jt < JT; ++jt)
+#pragma unroll
+      for (int nb = 0; nb < NT; ++nb)
+        acc[jt][nb][0] = acc[jt][nb][1] = acc[jt][nb][2] = acc[jt][nb][3] = 0.f;
+#pragma unroll
+    for (int jt = 0; jt < JT; ++jt) {
+      if (jt > 0 && j + jt >= wk.njobs) break;
+      if (!wt.wait_warp<false>(bars.full(stage), phase)) return;
+      const uint8_t* st = ring + stage * a.stage_bytes;
+      slice_xr<BITS, NT, GWM, NG, F16>(st + codes_off, st + scales_off, xr, lane, q, acc[jt]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.empty(stage));
+      if (++stage == a.stages) { stage = 0; phase ^= 1; }
     }
-    static_assert(GWM <= 5, "slice-length dispatch covers 1..5 groups");
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bars.empty(stage));
-    if (++stage == a.stages) { stage = 0; phase ^= 1; }
     if constexpr (F16) {
 #pragma unroll
-      for (int nb = 0; nb < NT; ++nb) {
-        acc[nb][0] *= inv[nb][0];
-        acc[nb][1] *= inv[nb][1];
-        acc[nb][2] *= inv16[nb][0];
-        acc[nb][3] *= inv16[nb][1];
-      }
+      for (int jt = 0; jt < JT; ++jt)
+#pragma unroll
+        for (int nb = 0; nb < NT; ++nb) {
+          acc[jt][nb][0] *= inv[nb][0];
+          acc[jt][nb][1] *= inv[nb][1];
+          acc[jt][nb][2] *= inv16[nb][0];
+          acc[jt][nb][3] *= inv16[nb][1];
+        }
     }
-    if (!hand_partial_mma<NT>(a, smem, bars, wt, warp, lane, rb, rn, acc)) return;
+    if (!hand_partials_mma<NT, JT>(a, smem, bars, wt, warp, lane, rb, rn, acc)) return;
     if (++rb == a.nbuf) { rb = 0; ++rn; }
   }
+}
+
+// The slice length n (uniform per warp, <= GWM) picks the job loop once.
+template <int BITS, int GWM, int NT, bool F16>
+__device__ __forceinline__ void run_xreg_jobs(const GemvArgs& a, uint8_t* smem, const Bars& bars,
+                                              const Waiter& wt, const Work& wk, int warp,
+                                              int lane, int n, int codes_off, int scales_off,
+                                              const uint32_t (&xr)[GWM][NT][8],
+                                              const float (&inv)[NT][2]) {
+  static_assert(GWM <= 5, "slice-length dispatch covers 1..5 groups");
+#define NQ_XREG_CASE(k)                                                                      \
+  case k:                                                                                    \
+    if constexpr (k <= GWM)                                                                  \
+      xreg_jobs<BITS, GWM, NT, F16, k>(a, smem, bars, wt, wk, warp, lane, codes_off,         \
+                                       scales_off, xr, inv);                                 \
+    break;
+  switch (n) {
+    NQ_XREG_CASE(1)
+    NQ_XREG_CASE(2)
+    NQ_XREG_CASE(3)
+    NQ_XREG_CASE(4)
+    NQ_XREG_CASE(5)
+    default:
+      // A warp without groups still takes part in every hand-off (zeros).
+      xreg_jobs<BITS, GWM, NT, F16, 0>(a, smem, bars, wt, wk, warp, lane, codes_off, scales_off,
+                                       xr, inv);
+      break;
+  }
+#undef NQ_XREG_CASE
 }
 
 // x in registers: a stage holds the CTA's whole K range of one job; the warp
@@ -807,13 +875,13 @@ __device__ void consumer_xreg(const GemvArgs& a, uint8_t* smem, const Bars& bars
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(smem + kXFreeBarOffset));
       if (f16) {
-        xreg_jobs<BITS, GWM, NT, true>(a, smem, bars, wt, wk, warp, lane, n, codes_off,
+        run_xreg_jobs<BITS, GWM, NT, true>(a, smem, bars, wt, wk, warp, lane, n, codes_off,
                                        scales_off, xr, inv);
         return;
       }
 #pragma unroll
       for (int nb = 0; nb < NT; ++nb) inv[nb][0] = inv[nb][1] = 1.f;
-      xreg_jobs<BITS, GWM, NT, false>(a, smem, bars, wt, wk, warp, lane, n, codes_off, scales_off,
+      run_xreg_jobs<BITS, GWM, NT, false>(a, smem, bars, wt, wk, warp, lane, n, codes_off, scales_off,
                                       xr, inv);
       return;
     }
@@ -821,7 +889,7 @@ __device__ void consumer_xreg(const GemvArgs& a, uint8_t* smem, const Bars& bars
   load_x_frags<GWM, NT>(a, sl, n, lane, xr);
 #pragma unroll
   for (int nb = 0; nb < NT; ++nb) inv[nb][0] = inv[nb][1] = 1.f;
-  xreg_jobs<BITS, GWM, NT, false>(a, smem, bars, wt, wk, warp, lane, n, codes_off, scales_off, xr,
+  run_xreg_jobs<BITS, GWM, NT, false>(a, smem, bars, wt, wk, warp, lane, n, codes_off, scales_off, xr,
                                   inv);
 }
 
@@ -973,8 +1041,10 @@ __device__ __forceinline__ void head_merge_lanes(float& m, float& s, int& a, int
   head_merge(m, s, a, mo, so, ao);
 }
 
-// End of a CTA's epilogue warp on the fused head: merge the four lanes of each
-// token and publish the warp's per-token states; then a two-level merge, each
+// End of a CTA's epilogue warp on the fused head: merge, per token, every
+// lane's states of that token (slot i of a lane holds token vtok[i]) with a
+// butterfly over the warp, and publish the warp's per-token states; then a
+// two-level merge, each
 // level done by the last warp to arrive and costing one round of loads:
 // the last warp of a group of kHeadGroup clusters merges the group's
 // 2 kHeadGroup states per token in (cluster, warp) order, and the last group
@@ -995,7 +1065,8 @@ __device__ __forceinline__ void head_merge_entries(const uint8_t* base, int firs
 
 template <int SLOTS>
 __device__ void head_finish(const GemvArgs& a, const Work& wk, int ew, int lane,
-                            float (&hm)[SLOTS], float (&hs)[SLOTS], int (&ha)[SLOTS]) {
+                            const float (&hm)[SLOTS], const float (&hs)[SLOTS],
+                            const int (&ha)[SLOTS], const int (&vtok)[SLOTS]) {
   const int T = a.T;
   const int cl = blockIdx.x / a.ksplit;
   const int grp = cl / kHeadGroup;
@@ -1005,15 +1076,18 @@ __device__ void head_finish(const GemvArgs& a, const Work& wk, int ew, int lane,
   unsigned* counters = reinterpret_cast<unsigned*>(a.h_ws);
   uint8_t* states = a.h_ws + kHeadCounterBytes;                  // (cluster, warp, token)
   uint8_t* gstates = states + static_cast<size_t>(a.clusters) * kEpiWarps * kHeadMaxT * kHeadStateBytes;
+  for (int t = 0; t < T; ++t) {
+    float m = -INFINITY, s = 0.f;
+    int am = INT_MAX;
 #pragma unroll
-  for (int i = 0; i < SLOTS; ++i) {
-    head_merge_lanes(hm[i], hs[i], ha[i], 1);
-    head_merge_lanes(hm[i], hs[i], ha[i], 2);
-    const int tok = (lane >> 2) + 8 * i;
-    if ((lane & 3) == 0 && tok < T) {
+    for (int i = 0; i < SLOTS; ++i)
+      if (vtok[i] == t) head_merge(m, s, am, hm[i], hs[i], ha[i]);
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) head_merge_lanes(m, s, am, d);
+    if (lane == 0) {
       const int me = cl * kEpiWarps + ew;
-      *reinterpret_cast<float4*>(states + (static_cast<size_t>(me) * kHeadMaxT + tok) * kHeadStateBytes) =
-          make_float4(hm[i], hs[i], __int_as_float(ha[i]), 0.f);
+      *reinterpret_cast<float4*>(states + (static_cast<size_t>(me) * kHeadMaxT + t) * kHeadStateBytes) =
+          make_float4(m, s, __int_as_float(am), 0.f);
     }
   }
   __threadfence();
@@ -1066,11 +1140,12 @@ __device__ void head_finish(const GemvArgs& a, const Work& wk, int ew, int lane,
   }
 }
 
-template <int SLOTS>
+template <int SLOTS, int JT>
 __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& bars,
                                 const Waiter& wt, const Work& wk, int ew, int lane) {
   const int T = a.T;
-  const int nv = 16 * T;             // values per row tile (a multiple of 16)
+  const int nvt = 16 * T;            // values per row tile (a multiple of 16)
+  const int nv = JT * nvt;           // values per hand-off (JT consecutive tiles)
   const int ks = a.ksplit;
   const float* red = reinterpret_cast<const float*>(smem + a.off_red);
   float* cl = reinterpret_cast<float*>(smem + a.off_cl);
@@ -1085,9 +1160,20 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
     hs[i] = 0.f;
     ha[i] = INT_MAX;
   }
-  int b = ew;        // buffer of job j (j % nbuf)
+  // Tile, token and row of this lane's four values in slot i (fixed per lane).
+  int vt[SLOTS], vtok[SLOTS], vrow[SLOTS];
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i) {
+    const int e = 4 * lane + 128 * i;
+    vt[i] = e / nvt;
+    const int rest = e - vt[i] * nvt;
+    vtok[i] = rest >> 4;
+    vrow[i] = rest & 15;
+  }
+  const int njt = (wk.njobs + JT - 1) / JT;  // hand-offs of this CTA
+  int b = ew;        // buffer of hand-off j (j % nbuf)
   uint32_t n = 0;    // uses of that buffer so far (j / nbuf)
-  for (int j = ew; j < wk.njobs; j += kEpiWarps) {
+  for (int j = ew; j < njt; j += kEpiWarps) {
     if (ks > 1 && wk.rank == 0 && lane == 0)
       mbar_arrive_expect_tx_relaxed(bars.cl_full(b), cl_bytes);
     if (!wt.wait_warp<false>(bars.red_full(b), n & 1u)) return;
@@ -1130,12 +1216,11 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
       }
     }
     if (store) {
-      const long long row0 = (wk.rt_begin + j) * 16;
 #pragma unroll
       for (int i = 0; i < SLOTS; ++i) {
-        const int e = 4 * lane + 128 * i;
-        if (has(i)) {
-          const int tok = e >> 4, row = e & 15;
+        if (has(i) && j * JT + vt[i] < wk.njobs) {
+          const long long row0 = (wk.rt_begin + j * JT + vt[i]) * 16;
+          const int tok = vtok[i], row = vrow[i];
           const long long nrow = a.N - (row0 + row);  // rows left in y from this one
           const float vv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
           if (a.y != nullptr) {
@@ -1155,7 +1240,7 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
     b += kEpiWarps;
     if (b >= a.nbuf) { b -= a.nbuf; ++n; }
   }
-  if (head && (ks == 1 || wk.rank == 0)) head_finish<SLOTS>(a, wk, ew, lane, hm, hs, ha);
+  if (head && (ks == 1 || wk.rank == 0)) head_finish<SLOTS>(a, wk, ew, lane, hm, hs, ha, vtok);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -1204,11 +1289,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const int ew = warp - kEpilogueWarp;
     griddep_wait();
     // Value slots per lane: 16 x T values over 32 lanes.
-    if constexpr (ROUTE == kRouteMma && (NTOK == 2 || NTOK == kNtokXreg2)) {
-      epilogue<2>(a, smem, bars, wt, wk, ew, lane);
-    } else {
-      epilogue<1>(a, smem, bars, wt, wk, ew, lane);
-    }
+    // Value slots per lane: JT x 16 x T values over 32 lanes, four each.
+    constexpr int JT = kJobTiles<ROUTE, NTOK>;
+    constexpr int kTokBlocks = (ROUTE == kRouteMma && (NTOK == 2 || NTOK == kNtokXreg2)) ? 2 : 1;
+    epilogue<JT * kTokBlocks, JT>(a, smem, bars, wt, wk, ew, lane);
   } else {
     griddep_wait();
     if constexpr (ROUTE == kRouteMma && NTOK == kNtokXreg) {

@@ -136,14 +136,18 @@ bool layout_for(const Plan& base, int G, int T, int bits, int ks, int sg, int mi
   const long long x_bytes =
       x_in_regs ? 0 : 1LL * gc_max * T * (p.route == NQ_ROUTE_MMA ? 128 : 256);
   // Partial-sum buffers in flight between the warps, the epilogue and the
-  // cluster's rank 0: deep for small T (cheap), shallow for large T.
+  // cluster's rank 0: deep for small T (cheap), shallow for large T.  The
+  // x-in-register kernels with one token block hand over two row tiles per
+  // buffer (JT = 2), so they need half as many buffers for the same slack.
   // (a multiple of kEpiWarps: each buffer belongs to one epilogue warp)
-  p.nbuf = T <= 2 ? kMaxBufs : T <= 4 ? 6 : T <= 8 ? 4 : 2;
+  const int jt = (x_in_regs && p.ntok == kNtokXreg) ? 2 : 1;   // the kernel's kJobTiles
+  if (jt == 2) p.nbuf = T <= 2 ? 4 : 2;
+  else p.nbuf = T <= 2 ? kMaxBufs : T <= 4 ? 6 : T <= 8 ? 4 : 2;
   static_assert(kMaxBufs % kEpiWarps == 0 && 6 % kEpiWarps == 0 && 4 % kEpiWarps == 0 &&
                     2 % kEpiWarps == 0,
                 "buffer counts must be multiples of the epilogue warps");
-  const int red_bytes = p.nbuf * kWarps * 16 * T * 4;
-  const int cl_bytes = ks > 1 ? p.nbuf * (ks - 1) * 16 * T * 4 : 0;
+  const int red_bytes = p.nbuf * kWarps * jt * 16 * T * 4;
+  const int cl_bytes = ks > 1 ? p.nbuf * (ks - 1) * jt * 16 * T * 4 : 0;
   p.stage_bytes = align_up(sg * (block_bytes(bits) + kScaleBytesPerBlock), 128);
   p.off_red = kBarRegionBytes;
   p.off_cl = p.off_red + align_up(red_bytes, 128);
