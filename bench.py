@@ -305,6 +305,56 @@ def fused_head_times(torch, nqp, entries, stream, reps):
     return out
 
 
+def mlp_times(torch, nqp, entries, stream, reps):
+    """One layer's MLP through nq_mlp (gate+up with SwiGLU in the epilogue,
+    then the down projection, programmatic dependent launch between them) at
+    every T, one CUDA graph per T, against the same two GEMVs launched plainly
+    (fp32 gate and up stored, no activation).  Weight bytes per layer / time.
+    (The stack's gate+up rows are not in the interleaved order a real layer
+    would use; the work, and so the time, is the same.)"""
+    gu = next(e for e in entries if e["kind"] == "gate_up")
+    dn = next(e for e in entries if e["kind"] == "down" and e["layer"] == 0)
+    dev = gu["x"].device
+    nbytes = (packed_bytes(gu["bits"], gu["K"], gu["N"]) + packed_bytes(dn["bits"], dn["K"], dn["N"]))
+    act = torch.empty((16, INTER), dtype=torch.int16, device=dev)
+    y1 = torch.empty((16, gu["N"]), dtype=torch.float32, device=dev)
+    y = torch.empty((16, dn["N"]), dtype=torch.float32, device=dev)
+    out = {}
+    for T in TS:
+        def fused():
+            nqp.mlp(gu["qw"], dn["qw"], gu["x"][:T], act[:T], y[:T], T, stream=stream)
+
+        def plain():
+            nqp.gemv(gu["qw"].packed, gu["qw"].scales, gu["x"][:T], y1[:T], gu["K"], gu["N"], T,
+                     gu["bits"], stream=stream)
+            nqp.gemv(dn["qw"].packed, dn["qw"].scales, act[:T].view(torch.bfloat16), y[:T], dn["K"],
+                     dn["N"], T, dn["bits"], stream=stream)
+        res = {}
+        for name, fn in (("fused_us", fused), ("two_gemv_us", plain)):
+            with torch.cuda.stream(stream):
+                fn()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                g.replay()
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+            stream.synchronize()
+            res[name] = round(e0.elapsed_time(e1) * 1e3 / reps, 2)
+        res["fused_gbs"] = round(nbytes / (res["fused_us"] * 1e-6) / 1e9, 1)
+        out[f"T{T}"] = res
+    rc = nqp.last_device_error(stream)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} in the MLP layer")
+    return out
+
+
 def encoder_times(torch, nqp, dev, reps=3):
     """Device round-to-nearest and searched encoders on one gate+up-sized
     fp32 matrix (K=5120, N=34816, 4-bit, synthetic imatrix), CUDA events; and
@@ -440,6 +490,9 @@ def run_ours(args, rank, world, local_rank):
     # ---------------- fused verify head (argmax, maximum, logsumexp per token)
     head_fused = fused_head_times(torch, nqp, entries, stream, reps=max(10, min(args.steps, 50)))
 
+    # ---------------- one decoder-layer MLP: SwiGLU product then down (nq_mlp)
+    mlp_layer = mlp_times(torch, nqp, entries, stream, reps=max(10, min(args.steps, 50)))
+
     # ---------------- offline encoders on one gate+up-sized matrix
     encoders = encoder_times(torch, nqp, dev) if rank == 0 else None
 
@@ -509,6 +562,7 @@ def run_ours(args, rank, world, local_rank):
         "per_T": per_t,
         "kernels": kernels,
         "head_fused": head_fused,
+        "mlp_layer": mlp_layer,
         "encoders": encoders,
         "plans": {f"{k}_T{T}": nqp.plan(e["K"], e["N"], T, e["bits"])
                   for T in TS for k in kinds

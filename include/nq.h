@@ -159,6 +159,31 @@ int nq_gemv(const void* packed, const uint16_t* scales, const void* x_bf16, floa
 int nq_gemv_ex(const void* packed, const uint16_t* scales, const void* x_bf16, float* y,
                int64_t K, int64_t N, int T, int bits, int route, int ksplit, nq_stream_t stream);
 
+/* Gate+up product with the SwiGLU activation in its epilogue: the first half
+ * of the decoder layer's MLP (pages "giveen/ninfer-ext", section "Where
+ * ninfer-ext leads": the fused gate+up matrix; "Qwen3.8-27B for NInfer on the
+ * RTX 3090": Q4 gate/up projections), act[t, i] = bf16(silu(g) * u) with
+ * g = (x W_gate^T)[t, i], u = (x W_up^T)[t, i], silu(g) = g / (1 + exp(-g)),
+ * computed in fp32 and rounded to nearest-even bf16 (the input of the down
+ * projection).  The gate+up matrix must be packed (nq_pack / nq_pack_device)
+ * with its N = 2 I rows interleaved per 8: packed row 16 r + m is gate row
+ * 8 r + m and packed row 16 r + 8 + m is up row 8 r + m (m < 8), so gate and
+ * up of an index finish in the same row tile; N must be a multiple of 16.
+ * x_bf16: device [T, K]; act_bf16: device bf16 bit patterns [T, N / 2],
+ * written; the fp32 gate and up outputs never leave the chip. */
+int nq_gemv_swiglu(const void* packed_gu, const uint16_t* scales_gu, const void* x_bf16,
+                   void* act_bf16, int64_t K, int64_t N, int T, int bits, nq_stream_t stream);
+
+/* The decoder layer's MLP on the stream: act = nq_gemv_swiglu(x) then
+ * y[T, H_out] = act W_down^T (nq_gemv; the second launch overlaps the first's
+ * tail by programmatic dependent launch).  H = K of gate+up, I = intermediate
+ * size (gate+up has 2 I rows, interleaved as above; down has H_out rows and
+ * K = I, a multiple of 64); act_bf16: device scratch [T, I] bf16 owned by the
+ * caller (the intermediate, 2 I T bytes). */
+int nq_mlp(const void* packed_gu, const uint16_t* scales_gu, int bits_gu, const void* packed_down,
+           const uint16_t* scales_down, int bits_down, const void* x_bf16, void* act_bf16,
+           float* y, int64_t H, int64_t I, int64_t H_out, int T, nq_stream_t stream);
+
 /* Fused verify head: the product of nq_gemv (y may be NULL: logits not
  * stored) and, per token t < T, over the N outputs y[t, 0..N):
  *   argmax[t] = the smallest n with y[t, n] maximal (int32; -1 if every

@@ -96,6 +96,25 @@ def f64_to_fp16_bits(v) -> np.ndarray:
         return np.asarray(v, dtype=np.float64).astype(np.float16).view(np.uint16)
 
 
+BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
+
+
+def f64_to_bf16_bits(v) -> np.ndarray:
+    """IEEE round-to-nearest-even of float64 values to bfloat16 bit patterns in
+    one rounding: 8 significant bits, step 2^-133 below the normal range,
+    overflow to infinity."""
+    x = np.asarray(v, dtype=np.float64)
+    fin = np.isfinite(x)
+    xf = np.where(fin, x, 0.0)
+    _, e = np.frexp(xf)
+    q = np.ldexp(1.0, np.maximum(e - 8, -133))
+    r = np.rint(xf / q) * q
+    with np.errstate(over="ignore"):
+        r = np.where(np.abs(r) > BF16_MAX, np.copysign(np.inf, xf), r)
+    r = np.where(fin, r, x)
+    return (r.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
 # --------------------------------------------------------------------------
 # Round-to-nearest encoder ("upstream" encoder on the 3090 model card).
 # Pin: exact rational nearest-FP16 search for the scale, brute-force nearest
@@ -278,6 +297,34 @@ def head_reduce(y):
     m = y[np.arange(y.shape[0]), am]
     lse = m + np.log(np.sum(np.exp(y - m[:, None]), axis=1))
     return am, m, lse
+
+
+# --------------------------------------------------------------------------
+# MLP of the decoder layer (page "giveen/ninfer-ext", fused gate+up; page
+# "Qwen3.8-27B for NInfer on the RTX 3090", Q4 gate/up and down projections):
+# act = silu(gate) * up with silu(g) = g / (1 + exp(-g)), rounded to bf16
+# because it is the bf16 input of the down projection; y = act W_down^T.
+# --------------------------------------------------------------------------
+def silu(g):
+    g = np.asarray(g, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g))
+
+
+def swiglu_bf16(gate, up):
+    """bf16 bit patterns of silu(gate) * up, computed in fp64, rounded once."""
+    return f64_to_bf16_bits(silu(gate) * np.asarray(up, dtype=np.float64))
+
+
+def mlp(codes_gu, scales_gu, codes_down, scales_down, x_bits):
+    """The layer's MLP on x [T, H] (bf16 bits): gate+up [2I, H] in (gate; up)
+    row order, act [T, I] (bf16 bits), y [T, H'] and the down product's error
+    scale E = sum |w act|.  Returns (act_bits, y, E, gate, up, E_gate, E_up)."""
+    y_gu, e_gu = gemv(codes_gu, scales_gu, x_bits)
+    i = y_gu.shape[1] // 2
+    act = swiglu_bf16(y_gu[:, :i], y_gu[:, i:])
+    y, e = gemv(codes_down, scales_down, act)
+    return act, y, e, y_gu[:, :i], y_gu[:, i:], e_gu[:, :i], e_gu[:, i:]
 
 
 # --------------------------------------------------------------------------

@@ -19,7 +19,7 @@ import numpy as np
 
 __all__ = [
     "NQError", "ROUTE_AUTO", "ROUTE_MMA", "ROUTE_FFMA", "lib", "lib_path", "build",
-    "packed_bytes", "pack", "unpack", "pack_device", "quantize_rtn", "quantize_search", "gemv", "gemv_head",
+    "packed_bytes", "pack", "unpack", "pack_device", "quantize_rtn", "quantize_search", "gemv", "gemv_swiglu", "mlp", "interleave_gate_up", "gemv_head",
     "head_workspace_bytes", "gemv_head_noalloc", "dequant",
     "last_device_error", "plan", "selftest_wait_timeout", "status_string", "layout_version",
     "QuantizedWeight", "EXPORTED",
@@ -45,6 +45,8 @@ _SIGS = {
     "nq_quantize_search": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp]),
     "nq_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "nq_gemv_ex": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp]),
+    "nq_gemv_swiglu": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
+    "nq_mlp": (_i32, [_vp, _vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
     "nq_gemv_head": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp,
                             ctypes.c_size_t, _vp]),
     "nq_head_workspace_bytes": (_i32, [_szp]),
@@ -208,6 +210,39 @@ def gemv(packed, scales, x, y, K: int, N: int, T: int, bits: int, route: int = R
         rc = lib().nq_gemv_ex(_dptr(packed), _dptr(scales), _dptr(x), _dptr(y), K, N, T, bits,
                               route, ksplit, _stream_handle(stream))
     _check(rc, "nq_gemv")
+
+
+def interleave_gate_up(gate, up):
+    """Rows of the gate+up matrix in the order nq_gemv_swiglu expects: row
+    16 r + m = gate row 8 r + m, row 16 r + 8 + m = up row 8 r + m (m < 8).
+    Works on numpy arrays or torch tensors [I, ...] (I a multiple of 8)."""
+    i = gate.shape[0]
+    rest = tuple(gate.shape[1:])
+    g = gate.reshape((i // 8, 1, 8) + rest)
+    u = up.reshape((i // 8, 1, 8) + rest)
+    try:
+        import torch
+        if isinstance(gate, torch.Tensor):
+            return torch.cat([g, u], dim=1).reshape((2 * i,) + rest)
+    except ImportError:
+        pass
+    import numpy as np
+    return np.concatenate([g, u], axis=1).reshape((2 * i,) + rest)
+
+
+def gemv_swiglu(packed_gu, scales_gu, x, act, K: int, N: int, T: int, bits: int, stream=None):
+    """act[T, N/2] (bf16 tensor) = silu(gate) * up from a gate+up matrix packed
+    with interleave_gate_up's row order."""
+    _check(lib().nq_gemv_swiglu(_dptr(packed_gu), _dptr(scales_gu), _dptr(x), _dptr(act), K, N, T,
+                                bits, _stream_handle(stream)), "nq_gemv_swiglu")
+
+
+def mlp(gu, down, x, act, y, T: int, stream=None):
+    """The layer MLP: gu, down are QuantizedWeight (gu packed interleaved);
+    act [T, I] bf16 scratch, y [T, H_out] fp32."""
+    _check(lib().nq_mlp(_dptr(gu.packed), _dptr(gu.scales), gu.bits, _dptr(down.packed),
+                        _dptr(down.scales), down.bits, _dptr(x), _dptr(act), _dptr(y), gu.K,
+                        gu.N // 2, down.N, T, _stream_handle(stream)), "nq_mlp")
 
 
 def head_workspace_bytes() -> int:

@@ -111,6 +111,11 @@ struct GemvArgs {
   int* h_argmax;
   float* h_max;
   float* h_lse;
+  // SwiGLU epilogue (act != nullptr): the matrix is a gate+up matrix packed
+  // with rows interleaved per 8 (tile r = gate rows 8r..8r+7, then up rows
+  // 8r..8r+7), and act[t, i] = bf16(silu(gate) * up) replaces y
+  // ([T, N / 2] bf16 bits, N a multiple of 16).
+  uint16_t* act;
 };
 constexpr int kHeadCounterBytes = 256;
 constexpr int kHeadStateBytes = 16;
@@ -998,6 +1003,10 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, const float4&
                ::"r"(cluster_addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(cluster_bar)
                : "memory");
 }
+// silu(g) * u in fp32: g / (1 + exp(-g)) * u (expf; -0 for very negative g).
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return g / (1.f + expf(-g)) * u;
+}
 __device__ __forceinline__ void add4(float4& a, const float4& b) {
   a.x += b.x;
   a.y += b.y;
@@ -1215,7 +1224,28 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
         }
       }
     }
-    if (store) {
+    if (store && a.act != nullptr) {
+      // Lanes 4m + {0, 1} hold gate rows 0..7 of their tile and token, lanes
+      // 4m + {2, 3} the up rows of the same indices (rows 8..15).
+      const long long ni = a.N >> 1;
+#pragma unroll
+      for (int i = 0; i < SLOTS; ++i) {
+        float4 up;
+        up.x = __shfl_down_sync(0xffffffffu, v[i].x, 2);
+        up.y = __shfl_down_sync(0xffffffffu, v[i].y, 2);
+        up.z = __shfl_down_sync(0xffffffffu, v[i].z, 2);
+        up.w = __shfl_down_sync(0xffffffffu, v[i].w, 2);
+        if (has(i) && (vrow[i] & 8) == 0 && j * JT + vt[i] < wk.njobs) {
+          const long long idx = (wk.rt_begin + j * JT + vt[i]) * 8 + vrow[i];
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(silu_mul(v[i].x, up.x), silu_mul(v[i].y, up.y));
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(silu_mul(v[i].z, up.z), silu_mul(v[i].w, up.w));
+          uint2 pk;
+          pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+          pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(a.act + vtok[i] * ni + idx) = pk;
+        }
+      }
+    } else if (store) {
 #pragma unroll
       for (int i = 0; i < SLOTS; ++i) {
         if (has(i) && j * JT + vt[i] < wk.njobs) {

@@ -343,7 +343,8 @@ struct HeadOut {
 };
 
 int launch_plan(const Plan& p, const void* packed, const uint16_t* scales, const void* x, float* y,
-                int64_t K, int64_t N, int T, cudaStream_t st, const HeadOut& head = HeadOut()) {
+                int64_t K, int64_t N, int T, cudaStream_t st, const HeadOut& head = HeadOut(),
+                uint16_t* act = nullptr) {
   DevInfo* d;
   if (int rc = dev_info(&d)) return rc;
   GemvArgs a;
@@ -374,6 +375,7 @@ int launch_plan(const Plan& p, const void* packed, const uint16_t* scales, const
   a.h_argmax = head.argmax;
   a.h_max = head.maxval;
   a.h_lse = head.lse;
+  a.act = act;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.clusters * p.ks));
@@ -676,6 +678,32 @@ int nq_gemv_head_noalloc(const void* packed, const uint16_t* scales, const void*
   // zero) on the stream before its launch.
   return nq_gemv_head(packed, scales, x_bf16, y, K, N, T, bits, argmax, maxval, lse, ws,
                       NQ_HEAD_SCRATCH_BYTES, stream);
+}
+
+int nq_gemv_swiglu(const void* packed_gu, const uint16_t* scales_gu, const void* x_bf16,
+                   void* act_bf16, int64_t K, int64_t N, int T, int bits, nq_stream_t stream) {
+  if (!packed_gu || !scales_gu || !x_bf16 || !act_bf16) return NQ_EINVAL;
+  if (int rc = check_shape(K, N, bits)) return rc;
+  if (T < 1 || T > kMaxT || N % 16 != 0) return NQ_EINVAL;
+  if (!aligned16(packed_gu) || !aligned16(scales_gu) || !aligned16(x_bf16) || !aligned16(act_bf16))
+    return NQ_EALIGN;
+  Plan p;
+  if (int rc = make_plan(K, N, T, bits, NQ_ROUTE_AUTO, 0, &p)) return rc;
+  return launch_plan(p, packed_gu, scales_gu, x_bf16, nullptr, K, N, T,
+                     reinterpret_cast<cudaStream_t>(stream), HeadOut(),
+                     static_cast<uint16_t*>(act_bf16));
+}
+
+int nq_mlp(const void* packed_gu, const uint16_t* scales_gu, int bits_gu, const void* packed_down,
+           const uint16_t* scales_down, int bits_down, const void* x_bf16, void* act_bf16,
+           float* y, int64_t H, int64_t I, int64_t H_out, int T, nq_stream_t stream) {
+  if (!packed_down || !scales_down || !y) return NQ_EINVAL;
+  if (I <= 0 || I % 64 != 0) return NQ_EINVAL;
+  if (int rc = check_shape(I, H_out, bits_down)) return rc;
+  if (!aligned16(packed_down) || !aligned16(scales_down) || !aligned16(y)) return NQ_EALIGN;
+  if (int rc = nq_gemv_swiglu(packed_gu, scales_gu, x_bf16, act_bf16, H, 2 * I, T, bits_gu, stream))
+    return rc;
+  return nq_gemv(packed_down, scales_down, act_bf16, y, I, H_out, T, bits_down, stream);
 }
 
 int nq_gemv_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, int* route_out,

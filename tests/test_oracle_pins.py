@@ -400,3 +400,46 @@ def test_search_importance_scale_invariance_and_overflow():
     big = np.full((1, 64), 7.0e5, np.float32)                     # every candidate > 65504
     with pytest.raises(ValueError):
         oracle.search_encode(big, 4)
+
+
+# ---------------------------------------------------------------- bf16 rounding, SwiGLU
+def test_bf16_rounding_identity_and_ties():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    finite = bits[(bits & 0x7F80) != 0x7F80]
+    v = oracle.bf16_to_f64(finite)
+    back = oracle.f64_to_bf16_bits(v)
+    # every finite bf16 value maps to itself (both zeros keep their sign)
+    assert np.array_equal(back, finite)
+    # midpoints between neighbours round to the even pattern (positive, normal)
+    lo = np.arange(0x0080, 0x7F7F, 7, dtype=np.uint16)
+    a, b = oracle.bf16_to_f64(lo), oracle.bf16_to_f64(lo + 1)
+    mid = (a + b) / 2.0                                        # exact in fp64
+    got = oracle.f64_to_bf16_bits(mid)
+    want = np.where(lo % 2 == 0, lo, lo + 1).astype(np.uint16)
+    assert np.array_equal(got, want)
+    assert oracle.f64_to_bf16_bits(np.array([3.5e38]))[0] == 0x7F80      # overflow
+    assert oracle.f64_to_bf16_bits(np.array([2.0 ** -134]))[0] == 0x0000  # half the subnormal step: to even (0)
+
+
+def test_bf16_rounding_nearest_in_exact_arithmetic():
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal(2000) * np.exp(rng.uniform(-30, 30, 2000))
+    r = oracle.bf16_to_f64(oracle.f64_to_bf16_bits(x))
+    for xi, ri in zip(x[:300], r[:300]):
+        m, e = np.frexp(xi)
+        q = Fraction(2) ** int(e - 8)
+        assert abs(Fraction(float(xi)) - Fraction(float(ri))) <= q / 2
+
+
+def test_silu_identities():
+    g = np.linspace(-30.0, 30.0, 601)
+    s = oracle.silu(g)
+    # silu(g) - silu(-g) = g and silu(0) = 0, silu(g) -> g for large g, -> 0 for very negative g
+    assert np.allclose(s - oracle.silu(-g), g, rtol=0, atol=1e-12)
+    assert oracle.silu(np.array([0.0]))[0] == 0.0
+    assert abs(oracle.silu(np.array([40.0]))[0] - 40.0) < 1e-15 * 40
+    assert abs(oracle.silu(np.array([-800.0]))[0]) == 0.0
+    # swiglu of (g, 1) is silu(g) rounded to bf16; (0, u) gives 0
+    act = oracle.swiglu_bf16(g, np.ones_like(g))
+    assert np.array_equal(act, oracle.f64_to_bf16_bits(s))
+    assert np.all(oracle.bf16_to_f64(oracle.swiglu_bf16(np.zeros(5), np.arange(5.0))) == 0.0)
