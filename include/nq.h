@@ -5,7 +5,10 @@
  * different from the upstream artifact"): a weight matrix W[N, K] is stored as
  * signed integer codes c in groups of 64 consecutive weights along K, with one
  * FP16 scale s per group, and w = s * c.  Code widths: 4 bits [-8, 7],
- * 5 bits [-16, 15], 6 bits [-32, 31].  Scales may be negative.  The library
+ * 5 bits [-16, 15], 6 bits [-32, 31], and 8 bits [-128, 127] (the 8-bit
+ * head and projections of the same engine: that page's section
+ * "Measurements" and page "jabbatheduck/ninfer-ext-models", table
+ * "Representation").  Scales may be negative.  The library
  * computes
  *
  *        y[t, n] = sum_k x[t, k] * s[n, k / 64] * c[n, k]      t < T <= 16
@@ -56,9 +59,10 @@
  *             take bits 0..3 of their code from bits 12..15 of word d and
  *             bits 4..5 from bits 12 + 2(d%2) .. 13 + 2(d%2) of word
  *             4 + d/2 (same offsets + 16 for the high code).
+ *     8 bits: word j holds pairs 2j, 2j+1; pair i at bit offset 8i.
  *   Inside a block, words 0..3 of all lanes come first (lane L at byte
  *   16 L), then the remaining words (lane L at 512 + 4(W-4) L).  Block size:
- *   512 / 640 / 768 bytes for 4 / 5 / 6 bits.  Blocks are ordered
+ *   512 / 640 / 768 / 1024 bytes for 4 / 5 / 6 / 8 bits.  Blocks are ordered
  *   [row tile][group]; codes bytes = Nt * G * block size.
  *   Scales: [row tile][group][8][2] FP16, entry (m, h) = row m + 8h of the
  *   tile; 32 bytes per block; scales bytes = Nt * G * 32.
@@ -90,11 +94,11 @@ typedef enum {
 typedef enum {
   NQ_ROUTE_AUTO = 0,     /* library choice (see NQ_ROUTE environment variable) */
   NQ_ROUTE_MMA = 1,      /* warp-level bf16 tensor-core MMA, fp32 accumulate, T <= 16 */
-  NQ_ROUTE_FFMA = 2      /* CUDA-core fp32 FMA, T <= 4 */
+  NQ_ROUTE_FFMA = 2      /* CUDA-core fp32 FMA, T <= 4, 4 to 6 bits */
 } nq_route;
 
 /* Byte sizes of the packed codes and packed scales of a W[N, K] tensor.
- * K % 64 == 0, K > 0, N > 0, bits in {4, 5, 6}; outputs are host pointers. */
+ * K % 64 == 0, K > 0, N > 0, bits in {4, 5, 6, 8}; outputs are host pointers. */
 int nq_packed_bytes(int64_t K, int64_t N, int bits, size_t* codes_bytes, size_t* scales_bytes);
 
 /* Host packer.  codes: host int8 [N, K] row-major, values in the signed range

@@ -50,7 +50,7 @@ __all__ = [
 ]
 
 GROUP = 64                       # weights per group along K
-QMAX = {4: 7, 5: 15, 6: 31}      # largest positive code per width
+QMAX = {4: 7, 5: 15, 6: 31, 8: 127}   # largest positive code per width
 
 
 def code_range(bits: int) -> tuple[int, int]:

@@ -73,6 +73,7 @@ cudaError_t launch_pack_device(const int8_t* codes, const uint16_t* scales, long
   switch (bits) {
     case 4: pack_kernel<4><<<grid, block, 0, st>>>(codes, scales, K, N, G, nthreads, out, scales_out); break;
     case 5: pack_kernel<5><<<grid, block, 0, st>>>(codes, scales, K, N, G, nthreads, out, scales_out); break;
+    case 8: pack_kernel<8><<<grid, block, 0, st>>>(codes, scales, K, N, G, nthreads, out, scales_out); break;
     default: pack_kernel<6><<<grid, block, 0, st>>>(codes, scales, K, N, G, nthreads, out, scales_out); break;
   }
   return cudaGetLastError();
@@ -97,14 +98,20 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ packed,
     words[i] = *reinterpret_cast<const uint32_t*>(base + lane_word_offset(BITS, lane, i));
 #pragma unroll
   for (int p = 0; p < 16; ++p) {
-    const uint32_t c2 = pair_codes_bf16<BITS>(words, p);
+    // bf16 codes from the GEMV's decode; 8-bit codes (wider than the bf16
+    // trick) straight from their fields
+    uint32_t c2;
+    if constexpr (BITS == 8) c2 = pair_field<8>(words, p);
+    else c2 = pair_codes_bf16<BITS>(words, p);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       int row, k;
       lane_code_coords(lane, p, h, &row, &k);
       const long long n = rt * kTileRows + row;
       if (n >= N) continue;
-      const float c = __uint_as_float(h == 0 ? (c2 << 16) : (c2 & 0xFFFF0000u));
+      float c;
+      if constexpr (BITS == 8) c = static_cast<float>(static_cast<int>((c2 >> (16 * h)) & 0xFFu) - 128);
+      else c = __uint_as_float(h == 0 ? (c2 << 16) : (c2 & 0xFFFF0000u));
       const uint16_t sb = scales[blk * 16 + 2 * (row & 7) + (row >> 3)];
       const float s = __half2float(__ushort_as_half(sb));
       w[n * K + static_cast<long long>(g) * kGroup + k] = s * c;
@@ -123,6 +130,7 @@ cudaError_t launch_dequant(const void* packed, const uint16_t* scales, float* w,
   switch (bits) {
     case 4: dequant_kernel<4><<<grid, block, 0, st>>>(in, scales, K, N, G, nthreads, w); break;
     case 5: dequant_kernel<5><<<grid, block, 0, st>>>(in, scales, K, N, G, nthreads, w); break;
+    case 8: dequant_kernel<8><<<grid, block, 0, st>>>(in, scales, K, N, G, nthreads, w); break;
     default: dequant_kernel<6><<<grid, block, 0, st>>>(in, scales, K, N, G, nthreads, w); break;
   }
   return cudaGetLastError();

@@ -327,6 +327,12 @@ __device__ __forceinline__ void load_lane_words(const uint8_t* blk, int lane, ui
   w[3] = v.w;
   if constexpr (BITS == 5) {
     w[4] = *reinterpret_cast<const uint32_t*>(blk + 512 + 4 * lane);
+  } else if constexpr (BITS == 8) {
+    const uint4 u = *reinterpret_cast<const uint4*>(blk + 512 + 16 * lane);
+    w[4] = u.x;
+    w[5] = u.y;
+    w[6] = u.z;
+    w[7] = u.w;
   } else if constexpr (BITS == 6) {
     const uint2 u = *reinterpret_cast<const uint2*>(blk + 512 + 8 * lane);
     w[4] = u.x;
@@ -396,6 +402,26 @@ __device__ __forceinline__ void q4_codes_f16(uint32_t w, uint32_t& a0, uint32_t&
   a3 = sub_f16x2(lop3_and_or(w8, 0x00F000F0u, kMagic), kHi);
 }
 
+// 8-bit codes: bf16 has 7 mantissa bits, so each biased code u = c + 128 is
+// split into its low nibble (0..15) and its high nibble minus 8 (-8..7):
+// c = 16 (hi - 8) + lo.  Both planes decode like 4-bit codes (one lop3 and one
+// bf16x2 subtract each); the group runs two MMA chains and combines them as
+// 16 D_hi + D_lo before the scale.
+__device__ __forceinline__ void q8_pair_planes(const uint32_t (&w)[8], int p, uint32_t& lo,
+                                               uint32_t& hi) {
+  const uint32_t x = w[p >> 1] >> (8 * (p & 1));
+  const uint32_t xl = lop3_and_or(x, 0x000F000Fu, kBf16Magic2);        // 128 + lo
+  const uint32_t xh = lop3_and_or(x >> 4, 0x000F000Fu, kBf16Magic2);   // 128 + hi
+  const __nv_bfloat162 vlo =
+      __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&xl),
+              __halves2bfloat162(__ushort_as_bfloat16(0x4300), __ushort_as_bfloat16(0x4300)));  // - 128
+  const __nv_bfloat162 vhi =
+      __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&xh),
+              __halves2bfloat162(__ushort_as_bfloat16(0x4308), __ushort_as_bfloat16(0x4308)));  // - 136
+  lo = *reinterpret_cast<const uint32_t*>(&vlo);
+  hi = *reinterpret_cast<const uint32_t*>(&vhi);
+}
+
 // ------------------------------------------------------------------ per-group math
 // One group of one row tile on the MMA route: decode the lane's 32 codes, four
 // chained MMAs against the x fragments (the first starts from zero), scale,
@@ -414,23 +440,39 @@ __device__ __forceinline__ void mma_group(const uint8_t* blk, const uint8_t* sc,
     xa[nb] = *reinterpret_cast<const uint4*>(xp[nb]);
     xb[nb] = *reinterpret_cast<const uint4*>(xp[nb] + 16);
   }
-  float d[NT][4];
+  float d[NT][4], dh[NT][4];   // dh: high-nibble plane of 8-bit codes
 #pragma unroll
   for (int js = 0; js < 4; ++js) {
-    const uint32_t a0 = pair_codes_bf16<BITS>(w, 4 * js + 0);
-    const uint32_t a1 = pair_codes_bf16<BITS>(w, 4 * js + 1);
-    const uint32_t a2 = pair_codes_bf16<BITS>(w, 4 * js + 2);
-    const uint32_t a3 = pair_codes_bf16<BITS>(w, 4 * js + 3);
+    uint32_t a0, a1, a2, a3, h0 = 0, h1 = 0, h2 = 0, h3 = 0;
+    if constexpr (BITS == 8) {
+      q8_pair_planes(w, 4 * js + 0, a0, h0);
+      q8_pair_planes(w, 4 * js + 1, a1, h1);
+      q8_pair_planes(w, 4 * js + 2, a2, h2);
+      q8_pair_planes(w, 4 * js + 3, a3, h3);
+    } else {
+      a0 = pair_codes_bf16<BITS>(w, 4 * js + 0);
+      a1 = pair_codes_bf16<BITS>(w, 4 * js + 1);
+      a2 = pair_codes_bf16<BITS>(w, 4 * js + 2);
+      a3 = pair_codes_bf16<BITS>(w, 4 * js + 3);
+    }
 #pragma unroll
     for (int nb = 0; nb < NT; ++nb) {
       const uint32_t b0 = js == 0 ? xa[nb].x : js == 1 ? xa[nb].z : js == 2 ? xb[nb].x : xb[nb].z;
       const uint32_t b1 = js == 0 ? xa[nb].y : js == 1 ? xa[nb].w : js == 2 ? xb[nb].y : xb[nb].w;
       if (js == 0) {
         mma_16816_zc(d[nb], a0, a1, a2, a3, b0, b1);
+        if constexpr (BITS == 8) mma_16816_zc(dh[nb], h0, h1, h2, h3, b0, b1);
       } else {
         mma_16816(d[nb], a0, a1, a2, a3, b0, b1);
+        if constexpr (BITS == 8) mma_16816(dh[nb], h0, h1, h2, h3, b0, b1);
       }
     }
+  }
+  if constexpr (BITS == 8) {
+#pragma unroll
+    for (int nb = 0; nb < NT; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) d[nb][e] = fmaf(16.f, dh[nb][e], d[nb][e]);
   }
   const float2 s = __half22float2(sh);
 #pragma unroll
@@ -496,21 +538,38 @@ __device__ __forceinline__ void mma_group_xr(const uint8_t* blk, const uint8_t* 
   uint32_t w[BITS];
   load_lane_words<BITS>(blk, lane, w);
   const float2 s = __half22float2(*reinterpret_cast<const __half2*>(sc + 4 * q));
-  float d[NT][4];
+  float d[NT][4], dh[NT][4];   // dh: high-nibble plane of 8-bit codes
 #pragma unroll
   for (int js = 0; js < 4; ++js) {
-    const uint32_t a0 = pair_codes_bf16<BITS>(w, 4 * js + 0);
-    const uint32_t a1 = pair_codes_bf16<BITS>(w, 4 * js + 1);
-    const uint32_t a2 = pair_codes_bf16<BITS>(w, 4 * js + 2);
-    const uint32_t a3 = pair_codes_bf16<BITS>(w, 4 * js + 3);
+    uint32_t a0, a1, a2, a3, h0 = 0, h1 = 0, h2 = 0, h3 = 0;
+    if constexpr (BITS == 8) {
+      q8_pair_planes(w, 4 * js + 0, a0, h0);
+      q8_pair_planes(w, 4 * js + 1, a1, h1);
+      q8_pair_planes(w, 4 * js + 2, a2, h2);
+      q8_pair_planes(w, 4 * js + 3, a3, h3);
+    } else {
+      a0 = pair_codes_bf16<BITS>(w, 4 * js + 0);
+      a1 = pair_codes_bf16<BITS>(w, 4 * js + 1);
+      a2 = pair_codes_bf16<BITS>(w, 4 * js + 2);
+      a3 = pair_codes_bf16<BITS>(w, 4 * js + 3);
+    }
 #pragma unroll
     for (int nb = 0; nb < NT; ++nb) {
       if (js == 0) {
         mma_16816_zc(d[nb], a0, a1, a2, a3, xr[nb][0], xr[nb][1]);
+        if constexpr (BITS == 8) mma_16816_zc(dh[nb], h0, h1, h2, h3, xr[nb][0], xr[nb][1]);
       } else {
         mma_16816(d[nb], a0, a1, a2, a3, xr[nb][2 * js], xr[nb][2 * js + 1]);
+        if constexpr (BITS == 8)
+          mma_16816(dh[nb], h0, h1, h2, h3, xr[nb][2 * js], xr[nb][2 * js + 1]);
       }
     }
+  }
+  if constexpr (BITS == 8) {
+#pragma unroll
+    for (int nb = 0; nb < NT; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) d[nb][e] = fmaf(16.f, dh[nb][e], d[nb][e]);
   }
 #pragma unroll
   for (int nb = 0; nb < NT; ++nb) {

@@ -14,7 +14,9 @@
 //     bf16 with exponent 2^7), and one bf16x2 FMA removes 128 + 2^(b-1);
 //   * 5- and 6-bit fields are packed three (resp. two) per 16-bit half, with
 //     the leftover bits of every half holding one (resp. four) extra pairs, so
-//     no bits are wasted: 5.0 / 6.0 bits per code on top of the scales.
+//     no bits are wasted: 5.0 / 6.0 bits per code on top of the scales;
+//   * 8-bit fields are the two bytes of each half (pair 2w + f at byte f of
+//     word w's halves).
 // This header is shared by the host packer, the device packer, the dequant
 // kernel and the GEMV kernels, so all of them agree on the format.
 #pragma once
@@ -59,6 +61,8 @@ NQ_HD void encode_lane(int bits, const uint32_t* u, uint32_t* w) {
       const int hs = 16 * h;
       if (bits == 4) {
         w[p >> 2] |= v << (4 * (p & 3) + hs);
+      } else if (bits == 8) {
+        w[p >> 1] |= v << (8 * (p & 1) + hs);
       } else if (bits == 5) {
         if (p < 15) {
           w[p / 3] |= v << (5 * (p % 3) + hs);
@@ -84,6 +88,8 @@ template <int BITS>
 NQ_HD uint32_t pair_field(const uint32_t (&w)[BITS], int p) {
   if constexpr (BITS == 4) {
     return (w[p >> 2] >> (4 * (p & 3))) & 0x000F000Fu;
+  } else if constexpr (BITS == 8) {
+    return (w[p >> 1] >> (8 * (p & 1))) & 0x00FF00FFu;
   } else if constexpr (BITS == 5) {
     if (p < 15) return (w[p / 3] >> (5 * (p % 3))) & 0x001F001Fu;
     uint32_t t = (w[0] >> 15) & 0x00010001u;

@@ -20,6 +20,7 @@ namespace nq {
 const void* gemv_kernel_q4(int route, int ntok);
 const void* gemv_kernel_q5(int route, int ntok);
 const void* gemv_kernel_q6(int route, int ntok);
+const void* gemv_kernel_q8(int route, int ntok);
 cudaError_t launch_pack_device(const int8_t*, const uint16_t*, long long, long long, int, void*,
                                uint16_t*, cudaStream_t);
 cudaError_t launch_dequant(const void*, const uint16_t*, float*, long long, long long, int,
@@ -85,7 +86,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int check_shape(int64_t K, int64_t N, int bits) {
   if (K <= 0 || N <= 0 || K % kGroup != 0) return NQ_EINVAL;
-  if (bits < 4 || bits > 6) return NQ_EINVAL;
+  if (bits < 4 || bits > 8 || bits == 7) return NQ_EINVAL;
   if (K / kGroup > (1LL << 30) || N > (1LL << 40)) return NQ_EINVAL;
   return NQ_OK;
 }
@@ -108,6 +109,7 @@ const void* kernel_for(int bits, int route, int ntok) {
   switch (bits) {
     case 4: return gemv_kernel_q4(route, ntok);
     case 5: return gemv_kernel_q5(route, ntok);
+    case 8: return gemv_kernel_q8(route, ntok);
     default: return gemv_kernel_q6(route, ntok);
   }
 }
@@ -260,6 +262,7 @@ int make_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, Plan
   if (route == NQ_ROUTE_AUTO) route = NQ_ROUTE_MMA;
   if (route != NQ_ROUTE_MMA && route != NQ_ROUTE_FFMA) return NQ_EINVAL;
   if (route == NQ_ROUTE_FFMA && T > kFfmaMaxT) return NQ_EINVAL;
+  if (route == NQ_ROUTE_FFMA && bits == 8) return NQ_EINVAL;  // 8-bit codes: MMA route only
   if (ksplit == 0) ksplit = env_int("NQ_KSPLIT", 0);
   if (ksplit != 0 && ksplit != 1 && ksplit != 2 && ksplit != 4 && ksplit != 8) return NQ_EINVAL;
 
@@ -517,6 +520,7 @@ int nq_pack(const int8_t* codes, const uint16_t* scales, int64_t K, int64_t N, i
   switch (bits) {
     case 4: pack_host<4>(codes, scales, K, N, out, scales_out); break;
     case 5: pack_host<5>(codes, scales, K, N, out, scales_out); break;
+    case 8: pack_host<8>(codes, scales, K, N, out, scales_out); break;
     default: pack_host<6>(codes, scales, K, N, out, scales_out); break;
   }
   return NQ_OK;
@@ -530,6 +534,7 @@ int nq_unpack(const void* packed, const uint16_t* scales_packed, int64_t K, int6
   switch (bits) {
     case 4: unpack_host<4>(in, scales_packed, K, N, codes_out, scales_out); break;
     case 5: unpack_host<5>(in, scales_packed, K, N, codes_out, scales_out); break;
+    case 8: unpack_host<8>(in, scales_packed, K, N, codes_out, scales_out); break;
     default: unpack_host<6>(in, scales_packed, K, N, codes_out, scales_out); break;
   }
   return NQ_OK;

@@ -156,3 +156,20 @@ def test_head_full_size(T):
     codes, sb = oracle_inputs(case, rows)
     y_ref, e_ref = oracle.gemv(codes, sb, case["xb"][:T])
     assert oracle.max_violation(y[:, rows], y_ref, e_ref) <= 1.0
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("bits,T", [(4, 8), (6, 1), (8, 2)])
+def test_head_proposal_head_shape(bits, T):
+    """The 131,072-row proposal head (K = 5120): fused results against the
+    kernel's own logits, logits of sampled rows against the oracle."""
+    K, N = 5120, 131072
+    case = rtn_case((505, bits, T), bits, N, K, T)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    y, am, mx, lse = _head(case, packed, sp)
+    _check_self(y, am, mx, lse)
+    rng = np.random.default_rng(4)
+    rows = np.unique(np.concatenate([am, rng.choice(N, 256, replace=False)]))
+    codes, sb = oracle_inputs(case, rows)
+    y_ref, e_ref = oracle.gemv(codes, sb, case["xb"][:T])
+    assert oracle.max_violation(y[:, rows], y_ref, e_ref) <= 1.0

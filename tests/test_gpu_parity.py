@@ -45,7 +45,7 @@ def _check(case, y, rows=None):
 
 
 # ---------------------------------------------------------------- encoder, packers, dequant
-@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 def test_quantize_rtn_bit_exact(bits):
     case = rtn_case((300, bits), bits, 96, 512, 1)
     w = case["w"]
@@ -67,7 +67,7 @@ def test_quantize_rtn_overflow_sets_status():
     assert nqp.last_device_error() == 0              # read clears
 
 
-@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 def test_pack_device_matches_host_pack(bits):
     case = uniform_case((301, bits), bits, 53, 320, 1)
     codes, sb = oracle_inputs(case)
@@ -79,7 +79,7 @@ def test_pack_device_matches_host_pack(bits):
     assert np.array_equal(ds.cpu().numpy().view(np.uint16), hs)
 
 
-@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 @pytest.mark.parametrize("kind", ["rtn", "uniform"])
 def test_dequant_bit_exact(bits, kind):
     mk = rtn_case if kind == "rtn" else uniform_case
@@ -91,7 +91,7 @@ def test_dequant_bit_exact(bits, kind):
     assert np.array_equal(w.view(np.uint32), ref.view(np.uint32))
 
 
-@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 def test_dequant_every_scale_pattern(bits):
     # all 63,488 finite FP16 scale patterns x codes cycling through the range
     finite = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
@@ -114,7 +114,7 @@ def test_dequant_every_scale_pattern(bits):
 SHAPES = [(512, 256), (1024, 200), (2048, 37), (64, 16), (192, 1)]
 
 
-@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 @pytest.mark.parametrize("T", [1, 2, 3, 8, 9, 16])
 def test_gemv_mma_parity(bits, T):
     for i, (K, N) in enumerate(SHAPES):
@@ -162,7 +162,7 @@ def _upload_packed(codes, sb, bits):
     return torch.from_numpy(hp).to(DEV), torch.from_numpy(hs.view(np.int16)).to(DEV)
 
 
-@pytest.mark.parametrize("bits", [4, 6])
+@pytest.mark.parametrize("bits", [4, 6, 8])
 def test_one_hot_x_gives_weight_column_exactly(bits):
     case = uniform_case((307, bits), bits, 100, 1024, 4)
     codes, sb = oracle_inputs(case)
@@ -172,7 +172,8 @@ def test_one_hot_x_gives_weight_column_exactly(bits):
     for t, k in enumerate(ks_cols):
         xb[t, k] = 0x3F80
     c2 = dict(case, xb=xb, T=len(ks_cols))
-    for route, ks in ((nqp.ROUTE_MMA, 1), (nqp.ROUTE_MMA, 4), (nqp.ROUTE_FFMA, 2)):
+    routes = ((nqp.ROUTE_MMA, 1), (nqp.ROUTE_MMA, 4)) + (((nqp.ROUTE_FFMA, 2),) if bits < 8 else ())
+    for route, ks in routes:
         y = _y(c2, packed, sp, route=route, ksplit=ks, T=4)
         wref = oracle.dequant_f32(codes, sb)
         for t in range(4):
@@ -192,7 +193,7 @@ def test_zero_codes_and_negated_scales():
         assert np.array_equal(y1, -y2)
 
 
-@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 def test_t_invariance_exact(bits):
     case = rtn_case((309, bits), bits, 150, 1024, 16)
     packed, sp = device_weight(nqp, torch, case, DEV)
@@ -292,7 +293,7 @@ def test_invalid_arguments():
     x = device_x(torch, case, DEV)
     y = torch.empty((2, 32), dtype=torch.float32, device=DEV)
     bad = [dict(T=0), dict(T=17), dict(route=nqp.ROUTE_FFMA, T=5), dict(ksplit=3), dict(route=9),
-           dict(K=100), dict(bits=7)]
+           dict(K=100), dict(bits=7), dict(bits=8, route=nqp.ROUTE_FFMA)]
     for kw in bad:
         args = dict(K=128, N=32, T=2, bits=4, route=0, ksplit=0)
         args.update(kw)
@@ -331,6 +332,7 @@ FULL = {
     "gate_up_q4": ("rtn", 4, 34816, 5120, [1], 0.0),
     "down_q5": ("uniform", 5, 5120, 17408, [1, 8], 0.01),
     "head_q6": ("rtn", 6, 248320, 5120, [1, 2, 4, 8], 0.0),
+    "down_q8": ("rtn", 8, 5120, 17408, [1, 8, 16], 0.0),
 }
 SAMPLE_ROWS = 384
 
@@ -383,7 +385,7 @@ def test_full_size_sampled(full_cases, name):
 @pytest.mark.slow
 def test_full_size_graph_launch_path(full_cases):
     """The launch configuration the benchmark times: back-to-back GEMVs of the
-    three full-size shapes at T = 1, 8, 16 on a side stream, captured into one
+    full-size shapes at T = 1, 8, 16 on a side stream, captured into one
     CUDA graph (programmatic dependent launch between the kernels), replayed
     twice; sampled rows of every output against the oracle, and the two
     replays bitwise equal."""

@@ -48,7 +48,7 @@ def _structured(rng, k):
     return np.stack(rows).astype(np.float32)
 
 
-@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 def test_search_bit_exact(bits):
     rng = synth.generator(0, 910, bits)
     K = 1024
@@ -70,7 +70,7 @@ def test_search_overflow_sets_status():
     assert nqp.last_device_error() == 0
 
 
-@pytest.mark.parametrize("bits,T", [(4, 1), (5, 8), (6, 3)])
+@pytest.mark.parametrize("bits,T", [(4, 1), (5, 8), (6, 3), (8, 2)])
 def test_gemv_on_search_encoded_weights(bits, T):
     rng = synth.generator(0, 911, bits)
     N, K = 300, 2048

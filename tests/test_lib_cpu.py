@@ -32,7 +32,7 @@ def test_exports_every_header_symbol():
     assert nqp.layout_version() == 1
 
 
-@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 def test_packed_bytes(bits):
     cb, sb = nqp.packed_bytes(5120, 34816, bits)
     assert cb == 34816 * 5120 * bits // 8
@@ -47,6 +47,8 @@ def _spec_position(bits, lane, p, h):
     hs = 16 * h
     if bits == 4:
         return [(p // 4, 4 * (p % 4) + hs + m, m) for m in range(4)]
+    if bits == 8:
+        return [(p // 2, 8 * (p % 2) + hs + m, m) for m in range(8)]
     if bits == 5:
         if p < 15:
             return [(p // 3, 5 * (p % 3) + hs + m, m) for m in range(5)]
@@ -65,7 +67,7 @@ def _word(packed, bits, blk, lane, w):
     return int.from_bytes(bytes(packed[base + off: base + off + 4]), "little")
 
 
-@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 def test_pack_matches_header_spec(bits):
     rng = synth.generator(0, 200, bits)
     N, K = 40, 128                                   # 3 row tiles (last padded), 2 groups
@@ -96,7 +98,7 @@ def test_pack_matches_header_spec(bits):
                 assert sp[blk * 16 + 2 * (row % 8) + row // 8] == want
 
 
-@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 def test_roundtrip_every_code_in_every_position(bits):
     lo, hi = -(1 << (bits - 1)), (1 << (bits - 1)) - 1
     vals = np.arange(lo, hi + 1, dtype=np.int8)
@@ -115,7 +117,7 @@ def test_roundtrip_every_code_in_every_position(bits):
         assert (codes == v).any(axis=1).all()
 
 
-@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 def test_roundtrip_ragged(bits):
     rng = synth.generator(0, 202, bits)
     for N, K in [(1, 64), (17, 192), (255, 512)]:
@@ -126,19 +128,20 @@ def test_roundtrip_ragged(bits):
         assert np.array_equal(c2, codes) and np.array_equal(s2, scales)
 
 
-@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 def test_pack_rejects_out_of_range(bits):
     N, K = 16, 64
     codes = np.zeros((N, K), np.int8)
     scales = np.full((N, 1), 0x3C00, np.uint16)
-    codes[3, 5] = (1 << (bits - 1))                 # one above the range
-    with pytest.raises(nqp.NQError) as e:
-        nqp.pack(codes, scales, bits)
-    assert e.value.code == nqp.ERANGE
-    codes[3, 5] = -(1 << (bits - 1)) - 1
-    with pytest.raises(nqp.NQError):
-        nqp.pack(codes, scales, bits)
-    codes[3, 5] = 0
+    if bits < 8:                                    # every int8 is an 8-bit code
+        codes[3, 5] = (1 << (bits - 1))             # one above the range
+        with pytest.raises(nqp.NQError) as e:
+            nqp.pack(codes, scales, bits)
+        assert e.value.code == nqp.ERANGE
+        codes[3, 5] = -(1 << (bits - 1)) - 1
+        with pytest.raises(nqp.NQError):
+            nqp.pack(codes, scales, bits)
+        codes[3, 5] = 0
     for bad in (0x7C00, 0xFC00, 0x7E00):            # +inf, -inf, NaN
         s = scales.copy()
         s[2, 0] = bad

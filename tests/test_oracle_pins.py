@@ -74,7 +74,7 @@ def _nearest_fp16_exact(q: Fraction) -> int:
     return best[1]
 
 
-@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 def test_rtn_scale_is_exact_nearest_fp16(bits):
     rng = synth.generator(0, 100, bits)
     w = synth.gauss_weights(rng, 64, 64 * 8)
@@ -89,7 +89,7 @@ def test_rtn_scale_is_exact_nearest_fp16(bits):
             assert s[i, g] == _nearest_fp16_exact(q), (i, g)
 
 
-@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 def test_rtn_code_is_brute_force_nearest(bits):
     rng = synth.generator(0, 101, bits)
     n, k = 8, 256
@@ -105,7 +105,7 @@ def test_rtn_code_is_brute_force_nearest(bits):
             assert codes[i, j] == best, (i, j)
 
 
-@pytest.mark.parametrize("bits", [4, 5, 6])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 def test_rtn_invariants(bits):
     rng = synth.generator(0, 102, bits)
     w = synth.gauss_weights(rng, 64, 1024)
@@ -159,13 +159,13 @@ def test_worked_example_golden():
 def test_dequant_exact_all_fp16_times_all_codes():
     finite = ALL16[(ALL16 & 0x7C00) != 0x7C00]
     s = oracle.fp16_to_f64(finite)[:, None]
-    c = np.arange(-32, 32, dtype=np.float64)[None, :]
+    c = np.arange(-128, 128, dtype=np.float64)[None, :]       # every code of every width (4..8 bits)
     p = s * c
-    # exact in fp32: casting to fp32 and back loses nothing
+    # exact in fp32: casting to fp32 and back loses nothing (11 x 8 significant bits)
     assert np.array_equal(p.astype(np.float32).astype(np.float64), p)
     # and the oracle's dequant gives exactly these products
-    codes = np.tile(np.arange(-32, 32, dtype=np.int8), (finite.size, 1))
-    w = oracle.dequant(codes, finite[:, None])
+    codes = np.tile(np.arange(-128, 128, dtype=np.int16).astype(np.int8), (finite.size, 1))
+    w = oracle.dequant(codes, np.repeat(finite[:, None], 4, axis=1))   # 4 groups, one scale per row
     assert np.array_equal(w, p)
     # signed zero: -0 scale times positive code is -0
     assert np.signbit(oracle.dequant(np.full((1, 64), 3, np.int8), np.array([[0x8000]], np.uint16)))[0, 0]
