@@ -268,37 +268,58 @@ def build_stack(torch, nqp, dev, seed):
     return entries, x_arena, ys
 
 
+def _graph_us(torch, stream, run, reps):
+    """Average microseconds of `run` captured into one CUDA graph, replayed
+    `reps` times back to back on `stream` (one warm replay first)."""
+    with torch.cuda.stream(stream):
+        run()                      # plans and kernel attributes set before capture
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / reps
+
+
 def fused_head_times(torch, nqp, entries, stream, reps):
     """The output head through nq_gemv_head at every T (argmax, maximum and
-    logsumexp per token, logits not stored), one CUDA graph per T: average
+    logsumexp per token, logits not stored), and through nq_gemv_head_topk
+    with k = 8 and k = 32 (the same plus the top k per token; the merge
+    kernel included), one CUDA graph per call kind and T: average
     microseconds per call and weight-stream GB/s."""
     e = next(x for x in entries if x["kind"] == "head")
-    ws = torch.empty(nqp.head_workspace_bytes(), dtype=torch.uint8, device=e["x"].device)
+    dev = e["x"].device
+    ws = torch.empty(nqp.head_topk_workspace_bytes(), dtype=torch.uint8, device=dev)
     out = {}
     for T in TS:
-        res = [torch.empty(T, dtype=dt, device=ws.device) for dt in (torch.int32, torch.float32, torch.float32)]
+        res = [torch.empty(T, dtype=dt, device=dev) for dt in (torch.int32, torch.float32, torch.float32)]
+        tk_idx = torch.empty(T * 32, dtype=torch.int32, device=dev)    # [T, k] row-major
+        tk_val = torch.empty(T * 32, dtype=torch.float32, device=dev)
 
-        def run():
+        def head():
             nqp.gemv_head(e["qw"].packed, e["qw"].scales, e["x"][:T], e["K"], e["N"], T, e["bits"],
                           workspace=ws, argmax=res[0], maxval=res[1], lse=res[2], stream=stream)
-        with torch.cuda.stream(stream):
-            run()
-        stream.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            run()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            g.replay()
-            e0.record(stream)
-            for _ in range(reps):
-                g.replay()
-            e1.record(stream)
-        stream.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / reps
+
+        def topk(k):
+            def run():
+                nqp.gemv_head_topk(e["qw"].packed, e["qw"].scales, e["x"][:T], e["K"], e["N"], T,
+                                   e["bits"], k, workspace=ws, topk_idx=tk_idx[:T * k].view(T, k),
+                                   topk_val=tk_val[:T * k].view(T, k), argmax=res[0], maxval=res[1],
+                                   lse=res[2], stream=stream)
+            return run
+        us = _graph_us(torch, stream, head, reps)
         out[f"T{T}"] = {"us_per_call": round(us, 2),
                         "gbs": round(KIND_BYTES["head"] / (us * 1e-6) / 1e9, 1)}
+        for k in (8, 32):
+            out[f"T{T}"][f"topk{k}_us_per_call"] = round(_graph_us(torch, stream, topk(k), reps), 2)
     rc = nqp.last_device_error(stream)
     if rc != 0:
         raise RuntimeError(f"device status {rc} in the fused head")

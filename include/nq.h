@@ -196,7 +196,7 @@ int nq_mlp(const void* packed_gu, const uint16_t* scales_gu, int bits_gu, const 
  * These are the greedy-acceptance and normalisation values of a
  * speculative-verify round over the output head: the pages "giveen/ninfer-ext"
  * (section "Engineering", single-pass logsumexp) and "Qwen3.8-27B for NInfer
- * on the RTX 3090" (section "Artifact": candidate top-k over the full head).
+ * on the RTX 3090" (section "Run it": candidate top-k over the full head).
  * argmax, maxval, lse: device arrays of T entries, written when the stream
  * reaches the end of the call.  workspace: device scratch of at least
  * nq_head_workspace_bytes() bytes, 16-byte aligned, owned by the caller, any
@@ -210,6 +210,30 @@ int nq_gemv_head(const void* packed, const uint16_t* scales, const void* x_bf16,
 
 /* Bytes of workspace nq_gemv_head needs on the current device (any T, N). */
 int nq_head_workspace_bytes(size_t* bytes);
+
+/* nq_gemv_head plus the top k logits of every token: the drafter's candidate
+ * top-k over the output head of a speculative-verify round (page
+ * "Qwen3.8-27B for NInfer on the RTX 3090", section "Run it": the
+ * candidate top-k reads the proposal head or the full head; the pages do not
+ * fix k).  For t < T and j < k, topk_idx[t * k + j] / topk_val[t * k + j] is
+ * the j-th logit of token t in the order: larger fp32 value first, -0 just
+ * below +0, equal values by smaller row index (so the answer is unique; NaN
+ * logits rank by their bit pattern).  Entries beyond N (k > N) are index -1,
+ * value -inf.  The logits are not stored unless y is given; each epilogue
+ * warp keeps its own per-token top 32 while the product runs and a second
+ * kernel merges those lists, launched on the same stream.  1 <= k <= 32;
+ * topk_idx (int32) and topk_val (fp32): device arrays [T, k], row-major;
+ * workspace: device scratch of at least nq_head_topk_workspace_bytes()
+ * bytes, 16-byte aligned, owned by the caller, any contents on entry; calls
+ * sharing a workspace must be ordered.  argmax, maxval and lse as in
+ * nq_gemv_head.  Selection only: the result is deterministic. */
+int nq_gemv_head_topk(const void* packed, const uint16_t* scales, const void* x_bf16, float* y,
+                      int64_t K, int64_t N, int T, int bits, int k, int32_t* topk_idx,
+                      float* topk_val, int32_t* argmax, float* maxval, float* lse,
+                      void* workspace, size_t workspace_bytes, nq_stream_t stream);
+
+/* Bytes of workspace nq_gemv_head_topk needs on the current device (any T, N, k). */
+int nq_head_topk_workspace_bytes(size_t* bytes);
 
 /* nq_gemv_head for callers that cannot allocate device memory: a library
  * plugged into a host runtime that owns every device allocation and hands it

@@ -285,7 +285,7 @@ def gemv_rows(codes_rows: np.ndarray, scale_rows: np.ndarray, x_bits: np.ndarray
 # --------------------------------------------------------------------------
 # Verify-head reductions over the outputs of one token (page "giveen/ninfer-ext",
 # section "Engineering": single-pass logsumexp; page "Qwen3.8-27B for NInfer on
-# the RTX 3090", section "Artifact": candidate top-k over the full head).
+# the RTX 3090", section "Run it": candidate top-k over the full head).
 # --------------------------------------------------------------------------
 def head_reduce(y):
     """Per token t of y[T, N] (fp64): the argmax (first index of the largest
@@ -297,6 +297,28 @@ def head_reduce(y):
     m = y[np.arange(y.shape[0]), am]
     lse = m + np.log(np.sum(np.exp(y - m[:, None]), axis=1))
     return am, m, lse
+
+
+def head_topk(y, k):
+    """Per token t of y[T, N]: the k largest outputs as (index [T, k] int64,
+    value [T, k]) in the order larger value first, -0 below +0, equal values
+    by smaller index (the pages leave k and the order of ties open; this
+    reading makes the answer unique).  With k > N the tail is index -1, value
+    -inf.  A stable sort on (value descending, then the sign of zero), the
+    index order being kept by stability."""
+    y = np.asarray(y)
+    T, N = y.shape
+    idx = np.full((T, k), -1, dtype=np.int64)
+    val = np.full((T, k), -np.inf, dtype=y.dtype if y.dtype.kind == "f" else np.float64)
+    for t in range(T):
+        row = y[t]
+        # lexsort: last key primary.  Primary: value descending; secondary:
+        # +0 before -0 (signbit ascending); stability keeps index order.
+        order = np.lexsort((np.signbit(row), -row))
+        n = min(k, N)
+        idx[t, :n] = order[:n]
+        val[t, :n] = row[order[:n]]
+    return idx, val
 
 
 # --------------------------------------------------------------------------

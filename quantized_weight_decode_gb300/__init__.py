@@ -20,7 +20,8 @@ import numpy as np
 __all__ = [
     "NQError", "ROUTE_AUTO", "ROUTE_MMA", "ROUTE_FFMA", "lib", "lib_path", "build",
     "packed_bytes", "pack", "unpack", "pack_device", "quantize_rtn", "quantize_search", "gemv", "gemv_swiglu", "mlp", "interleave_gate_up", "gemv_head",
-    "head_workspace_bytes", "gemv_head_noalloc", "dequant",
+    "head_workspace_bytes", "gemv_head_noalloc", "gemv_head_topk", "head_topk_workspace_bytes",
+    "dequant",
     "last_device_error", "plan", "selftest_wait_timeout", "status_string", "layout_version",
     "QuantizedWeight", "EXPORTED",
 ]
@@ -50,6 +51,9 @@ _SIGS = {
     "nq_gemv_head": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp,
                             ctypes.c_size_t, _vp]),
     "nq_head_workspace_bytes": (_i32, [_szp]),
+    "nq_gemv_head_topk": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp, _vp, _vp,
+                                 _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "nq_head_topk_workspace_bytes": (_i32, [_szp]),
     "nq_gemv_head_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp,
                                     _vp]),
     "nq_dequant": (_i32, [_vp, _vp, _vp, _i64, _i64, _i32, _vp]),
@@ -273,6 +277,43 @@ def gemv_head(packed, scales, x, K: int, N: int, T: int, bits: int, y=None, work
                               workspace.numel() * workspace.element_size(),
                               _stream_handle(stream)), "nq_gemv_head")
     return argmax, maxval, lse
+
+
+def head_topk_workspace_bytes() -> int:
+    """Workspace bytes nq_gemv_head_topk needs on the current device."""
+    v = ctypes.c_size_t()
+    _check(lib().nq_head_topk_workspace_bytes(ctypes.byref(v)), "nq_head_topk_workspace_bytes")
+    return int(v.value)
+
+
+def gemv_head_topk(packed, scales, x, K: int, N: int, T: int, bits: int, k: int, y=None,
+                   workspace=None, topk_idx=None, topk_val=None, argmax=None, maxval=None,
+                   lse=None, stream=None):
+    """gemv_head plus the k largest logits of every token (larger value
+    first, equal values by smaller index).  Returns (topk_idx int32 [T, k],
+    topk_val fp32 [T, k], argmax, maxval, lse) device tensors; the workspace
+    and outputs not passed are allocated here (torch memory)."""
+    import torch
+    dev = x.device
+    if workspace is None:
+        workspace = torch.empty(head_topk_workspace_bytes(), dtype=torch.uint8, device=dev)
+    kk = max(k, 1)          # a bad k is the library's to reject
+    if topk_idx is None:
+        topk_idx = torch.empty((T, kk), dtype=torch.int32, device=dev)
+    if topk_val is None:
+        topk_val = torch.empty((T, kk), dtype=torch.float32, device=dev)
+    if argmax is None:
+        argmax = torch.empty(T, dtype=torch.int32, device=dev)
+    if maxval is None:
+        maxval = torch.empty(T, dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty(T, dtype=torch.float32, device=dev)
+    _check(lib().nq_gemv_head_topk(_dptr(packed), _dptr(scales), _dptr(x), _dptr(y), K, N, T, bits,
+                                   k, _dptr(topk_idx), _dptr(topk_val), _dptr(argmax),
+                                   _dptr(maxval), _dptr(lse), _dptr(workspace),
+                                   workspace.numel() * workspace.element_size(),
+                                   _stream_handle(stream)), "nq_gemv_head_topk")
+    return topk_idx, topk_val, argmax, maxval, lse
 
 
 def gemv_head_noalloc(packed, scales, x, K: int, N: int, T: int, bits: int, y=None,

@@ -50,6 +50,7 @@
 
 #include "layout.h"
 #include "ptx.cuh"
+#include "topk.cuh"
 
 namespace nq {
 
@@ -116,6 +117,16 @@ struct GemvArgs {
   // 8r..8r+7), and act[t, i] = bf16(silu(gate) * up) replaces y
   // ([T, N / 2] bf16 bits, N a multiple of 16).
   uint16_t* act;
+  // Top-k of the fused head (tk_k > 0, 1 <= tk_k <= kTopkMax): epilogue
+  // warp w of cluster c keeps, per token t, the 32 largest keys of the logits
+  // it finalised in tk_lists[((c * kEpiWarps + w) * kHeadMaxT + t) * 32 ...]
+  // (sorted descending; what the merge kernel reads), its candidate buffer in
+  // tk_bufs (64 keys per list, same indexing), and the buffer counts in
+  // shared memory at off_tk (kHeadMaxT ints per warp).
+  int tk_k;
+  int off_tk;
+  unsigned long long* tk_lists;
+  unsigned long long* tk_bufs;
 };
 constexpr int kHeadCounterBytes = 256;
 constexpr int kHeadStateBytes = 16;
@@ -1208,6 +1219,63 @@ __device__ void head_finish(const GemvArgs& a, const Work& wk, int ew, int lane,
   }
 }
 
+// Shared-memory bytes of the top-k buffer counts (all epilogue warps).
+constexpr int kTopkSmemBytes = kEpiWarps * kHeadMaxT * 4;
+
+// Folds the candidate buffer of token t (n keys, n < 64) into its list: at
+// most two rounds of sort 32 + merge.  Whole warp; list and buf are this
+// warp's own (global memory, written and read by this warp only).
+__device__ __forceinline__ void topk_flush(unsigned long long* list, unsigned long long* buf,
+                                           int* cnt, int t, int lane) {
+  const int n = cnt[t];
+  unsigned long long* lt = list + t * 32;
+  unsigned long long m = lt[lane];
+  for (int base = 0; base < n; base += 32) {
+    unsigned long long c = base + lane < n ? buf[t * 64 + base + lane] : 0ull;
+    c = warp_sort_desc(c, lane);
+    m = warp_top32_of_two(m, c, lane);
+  }
+  __syncwarp();
+  lt[lane] = m;
+  if (lane == 0) cnt[t] = 0;
+  __syncwarp();
+}
+
+// One hand-off's logits into the warp's top-k state (the selection scheme of
+// warp-level k-selection: cheap filtering against a threshold, sorting only
+// in batches).  A logit whose key beats the k-th key of its token's list
+// (a lower bound of the warp's k-th largest so far) is appended to the
+// token's buffer; a buffer holding 32 or more keys after the hand-off is
+// folded into the list.  A hand-off adds at most JT x 16 <= 32 keys per
+// token, so a buffer (64 keys) never overflows.  ok[i]: slot i holds logits
+// (rows rbase[i] .. rbase[i] + 3, those below N) of token vtok[i].
+template <int SLOTS>
+__device__ __forceinline__ void topk_update(const GemvArgs& a, unsigned long long* list,
+                                            unsigned long long* buf, int* cnt, int lane,
+                                            const float4 (&v)[SLOTS], const bool (&ok)[SLOTS],
+                                            const long long (&rbase)[SLOTS],
+                                            const int (&vtok)[SLOTS]) {
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i) {
+    if (!ok[i]) continue;
+    const int t = vtok[i];
+    const unsigned long long thr = list[t * 32 + a.tk_k - 1];
+    const float vv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const unsigned long long key = topk_key(vv[c], static_cast<uint32_t>(rbase[i] + c));
+      if (rbase[i] + c < a.N && key > thr) buf[t * 64 + atomicAdd(cnt + t, 1)] = key;
+    }
+  }
+  __syncwarp();
+  unsigned full = __ballot_sync(0xffffffffu, lane < a.T && cnt[lane] >= 32);
+  while (full) {
+    const int t = __ffs(full) - 1;
+    full &= full - 1;
+    topk_flush(list, buf, cnt, t, lane);
+  }
+}
+
 template <int SLOTS, int JT>
 __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& bars,
                                 const Waiter& wt, const Work& wk, int ew, int lane) {
@@ -1239,6 +1307,19 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
     vrow[i] = rest & 15;
   }
   const int njt = (wk.njobs + JT - 1) / JT;  // hand-offs of this CTA
+  const bool topk = head && a.tk_k > 0 && (ks == 1 || wk.rank == 0);
+  unsigned long long* tk_list = nullptr;
+  unsigned long long* tk_buf = nullptr;
+  int* tk_cnt = nullptr;
+  if (topk) {
+    const size_t me = static_cast<size_t>(blockIdx.x / ks) * kEpiWarps + ew;
+    tk_list = a.tk_lists + me * kHeadMaxT * 32;
+    tk_buf = a.tk_bufs + me * kHeadMaxT * 64;
+    tk_cnt = reinterpret_cast<int*>(smem + a.off_tk) + ew * kHeadMaxT;
+    for (int t = 0; t < T; ++t) tk_list[t * 32 + lane] = 0ull;  // empty keys
+    if (lane < T) tk_cnt[lane] = 0;
+    __syncwarp();
+  }
   int b = ew;        // buffer of hand-off j (j % nbuf)
   uint32_t n = 0;    // uses of that buffer so far (j / nbuf)
   for (int j = ew; j < njt; j += kEpiWarps) {
@@ -1325,9 +1406,23 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
           }
         }
       }
+      if (topk) {
+        bool ok[SLOTS];
+        long long rbase[SLOTS];
+#pragma unroll
+        for (int i = 0; i < SLOTS; ++i) {
+          ok[i] = has(i) && j * JT + vt[i] < wk.njobs;
+          rbase[i] = (wk.rt_begin + j * JT + vt[i]) * 16 + vrow[i];
+        }
+        topk_update<SLOTS>(a, tk_list, tk_buf, tk_cnt, lane, v, ok, rbase, vtok);
+      }
     }
     b += kEpiWarps;
     if (b >= a.nbuf) { b -= a.nbuf; ++n; }
+  }
+  if (topk) {
+    for (int t = 0; t < T; ++t)
+      if (tk_cnt[t] > 0) topk_flush(tk_list, tk_buf, tk_cnt, t, lane);
   }
   if (head && (ks == 1 || wk.rank == 0)) head_finish<SLOTS>(a, wk, ew, lane, hm, hs, ha, vtok);
 }

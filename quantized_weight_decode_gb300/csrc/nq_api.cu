@@ -30,6 +30,8 @@ cudaError_t launch_quantize_rtn(const float*, long long, long long, int, int8_t*
 cudaError_t launch_quantize_search(const float*, const float*, long long, long long, int, int8_t*,
                                    uint16_t*, int*, cudaStream_t);
 cudaError_t launch_selftest_timeout(unsigned long long, int*, cudaStream_t);
+cudaError_t launch_topk_merge(const unsigned long long*, int, int, int, int32_t*, float*, bool,
+                              cudaStream_t);
 int* device_status_ptr();
 
 namespace {
@@ -122,6 +124,7 @@ struct Plan {
   int route = 0, ntok = 0, ks = 1, clusters = 0, sg = 1, stages = 0, stage_bytes = 0, nbuf = 2;
   int smem = 0, off_ring = 0, off_red = 0, off_cl = 0, off_x = 0;
   int off_xh = -1, xh_stage0 = 0;  // fp16 x staging of the 4-bit x-in-register kernels
+  int off_tk = 0;                  // top-k lists of the fused head's epilogue warps
   const void* func = nullptr;
   double est_us = 0;
 };
@@ -129,7 +132,7 @@ struct Plan {
 // Shared-memory layout for a K-split and a stage size (64-groups per stage);
 // false if fewer than `min_stages` stages fit.
 bool layout_for(const Plan& base, int G, int T, int bits, int ks, int sg, int min_stages,
-                int smem_optin, Plan* out) {
+                int smem_optin, int extra, Plan* out) {
   Plan p = base;
   p.ks = ks;
   p.sg = sg;
@@ -154,8 +157,8 @@ bool layout_for(const Plan& base, int G, int T, int bits, int ks, int sg, int mi
   p.off_red = kBarRegionBytes;
   p.off_cl = p.off_red + align_up(red_bytes, 128);
   p.off_x = p.off_cl + align_up(cl_bytes, 128);
-  const long long fixed =
-      p.off_x + align_up(static_cast<int>(std::min<long long>(x_bytes, 1 << 30)), 128);
+  p.off_tk = p.off_x + align_up(static_cast<int>(std::min<long long>(x_bytes, 1 << 30)), 128);
+  const long long fixed = p.off_tk + align_up(extra, 128);
   if (fixed >= smem_optin) return false;
   p.off_ring = static_cast<int>(fixed);
   p.stages = static_cast<int>(std::min<long long>(kMaxStages, (smem_optin - fixed) / p.stage_bytes));
@@ -255,7 +258,10 @@ double estimate_us(const Plan& p, long long Nt, int G, int bits) {
   return t;
 }
 
-int make_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, Plan* out) {
+// extra: shared-memory bytes the epilogue needs besides the plain GEMV's (the
+// fused head's top-k lists), placed at Plan::off_tk.
+int make_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, Plan* out,
+              int extra = 0) {
   if (int rc = check_shape(K, N, bits)) return rc;
   if (T < 1 || T > kMaxT) return NQ_EINVAL;
   if (route == NQ_ROUTE_AUTO) route = env_route();
@@ -308,14 +314,14 @@ int make_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, Plan
     bool fit = false;
     if (route == NQ_ROUTE_MMA && gw_max <= xreg_max_groups) {
       // x held in registers; a stage is the CTA's whole K range of one job.
-      fit = layout_for(xreg, G, T, bits, ks, gc_max, 2, d->smem_optin, &p);
+      fit = layout_for(xreg, G, T, bits, ks, gc_max, 2, d->smem_optin, extra, &p);
     }
     // Otherwise x in shared memory; a stage is the job's K range cut into
     // `parts` equal pieces, the fewest that leave at least 3 stages (2 when
     // a piece is down to one group per warp).
     for (int parts = 1; !fit && parts <= gc_max; ++parts) {
       const int sg = (gc_max + parts - 1) / parts;
-      fit = layout_for(base, G, T, bits, ks, sg, sg <= kWarps ? 2 : 3, d->smem_optin, &p);
+      fit = layout_for(base, G, T, bits, ks, sg, sg <= kWarps ? 2 : 3, d->smem_optin, extra, &p);
       if (sg <= kWarps) break;
     }
     if (!fit) continue;
@@ -343,6 +349,9 @@ struct HeadOut {
   int32_t* argmax = nullptr;
   float* maxval = nullptr;
   float* lse = nullptr;
+  int tk_k = 0;                           // top-k (0: none)
+  unsigned long long* tk_lists = nullptr;
+  unsigned long long* tk_bufs = nullptr;
 };
 
 int launch_plan(const Plan& p, const void* packed, const uint16_t* scales, const void* x, float* y,
@@ -378,6 +387,10 @@ int launch_plan(const Plan& p, const void* packed, const uint16_t* scales, const
   a.h_argmax = head.argmax;
   a.h_max = head.maxval;
   a.h_lse = head.lse;
+  a.tk_k = head.tk_k;
+  a.off_tk = p.off_tk;
+  a.tk_lists = head.tk_lists;
+  a.tk_bufs = head.tk_bufs;
   a.act = act;
 
   cudaLaunchConfig_t cfg = {};
@@ -612,10 +625,14 @@ int nq_head_workspace_bytes(size_t* bytes) {
   return NQ_OK;
 }
 
-int nq_gemv_head(const void* packed, const uint16_t* scales, const void* x_bf16, float* y,
-                 int64_t K, int64_t N, int T, int bits, int32_t* argmax, float* maxval, float* lse,
-                 void* workspace, size_t workspace_bytes, nq_stream_t stream) {
+// Shared by the fused head entry points: validation, the arrival counter
+// clear, the head GEMV, and (k > 0) the top-k merge.
+static int head_launch(const void* packed, const uint16_t* scales, const void* x_bf16, float* y,
+                       int64_t K, int64_t N, int T, int bits, int32_t* argmax, float* maxval,
+                       float* lse, int k, int32_t* topk_idx, float* topk_val, void* workspace,
+                       size_t workspace_bytes, nq_stream_t stream) {
   if (!packed || !scales || !x_bf16 || !argmax || !maxval || !lse || !workspace) return NQ_EINVAL;
+  if (k < 0 || k > kTopkMax || (k > 0 && (!topk_idx || !topk_val))) return NQ_EINVAL;
   if (int rc = check_shape(K, N, bits)) return rc;
   if (T < 1 || T > kMaxT) return NQ_EINVAL;
   if (N > INT32_MAX) return NQ_EINVAL;  // row indices are int32
@@ -628,10 +645,13 @@ int nq_gemv_head(const void* packed, const uint16_t* scales, const void* x_bf16,
       (y && !aligned16(y)))
     return NQ_EALIGN;
   size_t need = 0;
-  if (int rc = nq_head_workspace_bytes(&need)) return rc;
+  if (int rc = (k > 0 ? nq_head_topk_workspace_bytes(&need) : nq_head_workspace_bytes(&need)))
+    return rc;
   if (workspace_bytes < need) return NQ_EINVAL;
   Plan p;
-  if (int rc = make_plan(K, N, T, bits, NQ_ROUTE_AUTO, 0, &p)) return rc;
+  if (int rc = make_plan(K, N, T, bits, NQ_ROUTE_AUTO, 0, &p,
+                         k > 0 ? kTopkSmemBytes : 0))
+    return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // The arrival counter must start at zero on every call (a call that gave up
   // on a bounded wait leaves it behind).
@@ -644,7 +664,52 @@ int nq_gemv_head(const void* packed, const uint16_t* scales, const void* x_bf16,
   h.argmax = argmax;
   h.maxval = maxval;
   h.lse = lse;
-  return launch_plan(p, packed, scales, x_bf16, y, K, N, T, st, h);
+  size_t head_bytes = 0;
+  if (k > 0) {
+    if (int rc = nq_head_workspace_bytes(&head_bytes)) return rc;
+    h.tk_k = k;
+    h.tk_lists = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) +
+                                                       align_up(static_cast<int>(head_bytes), 256));
+    DevInfo* d;
+    if (int rc = dev_info(&d)) return rc;
+    h.tk_bufs = h.tk_lists + static_cast<size_t>(d->sms) * kEpiWarps * kHeadMaxT * 32;
+  }
+  if (int rc = launch_plan(p, packed, scales, x_bf16, y, K, N, T, st, h)) return rc;
+  if (k > 0 && launch_topk_merge(h.tk_lists, p.clusters * kEpiWarps, T, k, topk_idx, topk_val,
+                                 env_int("NQ_PDL", 1) != 0, st) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return NQ_ECUDA;
+  }
+  return NQ_OK;
+}
+
+int nq_gemv_head(const void* packed, const uint16_t* scales, const void* x_bf16, float* y,
+                 int64_t K, int64_t N, int T, int bits, int32_t* argmax, float* maxval, float* lse,
+                 void* workspace, size_t workspace_bytes, nq_stream_t stream) {
+  return head_launch(packed, scales, x_bf16, y, K, N, T, bits, argmax, maxval, lse, 0, nullptr,
+                     nullptr, workspace, workspace_bytes, stream);
+}
+
+int nq_head_topk_workspace_bytes(size_t* bytes) {
+  if (!bytes) return NQ_EINVAL;
+  size_t head_bytes = 0;
+  if (int rc = nq_head_workspace_bytes(&head_bytes)) return rc;
+  DevInfo* d;
+  if (int rc = dev_info(&d)) return rc;
+  // then per (cluster, epilogue warp, token) a list of 32 keys, then a
+  // candidate buffer of 64 keys; clusters <= SMs
+  *bytes = static_cast<size_t>(align_up(static_cast<int>(head_bytes), 256)) +
+           static_cast<size_t>(d->sms) * kEpiWarps * kHeadMaxT * (32 + 64) * sizeof(unsigned long long);
+  return NQ_OK;
+}
+
+int nq_gemv_head_topk(const void* packed, const uint16_t* scales, const void* x_bf16, float* y,
+                      int64_t K, int64_t N, int T, int bits, int k, int32_t* topk_idx,
+                      float* topk_val, int32_t* argmax, float* maxval, float* lse,
+                      void* workspace, size_t workspace_bytes, nq_stream_t stream) {
+  if (k < 1) return NQ_EINVAL;
+  return head_launch(packed, scales, x_bf16, y, K, N, T, bits, argmax, maxval, lse, k, topk_idx,
+                     topk_val, workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------- fused head, no allocation

@@ -313,6 +313,57 @@ def test_head_rows_are_independent_tokens():
     assert np.all(np.abs(lse2 - (lse + 123.5)) <= 1e-12 * np.abs(lse2))
 
 
+def test_head_topk_worked_example():
+    # by hand: values 3 (rows 1, 2), 2 (row 5), 1 (row 0), +0 (row 4), -0 (row 3)
+    y = np.array([[1.0, 3.0, 3.0, -0.0, 0.0, 2.0]])
+    idx, val = oracle.head_topk(y, 8)
+    assert idx.tolist() == [[1, 2, 5, 0, 4, 3, -1, -1]]
+    assert val[0, :6].tolist() == [3.0, 3.0, 2.0, 1.0, 0.0, -0.0]
+    assert not np.signbit(val[0, 4]) and np.signbit(val[0, 5])
+    assert np.all(np.isneginf(val[0, 6:]))
+
+
+def test_head_topk_against_sorting_and_argmax():
+    rng = np.random.default_rng(9)
+    y = rng.standard_normal((5, 1000)).astype(np.float32)
+    y[2, 100:110] = y[2].max() + 1                         # a ten-way tie at the top
+    for k in (1, 7, 32):
+        idx, val = oracle.head_topk(y, k)
+        # the values are the k largest (a library sort, no index logic)
+        assert np.array_equal(val, -np.sort(-y, axis=1)[:, :k])
+        assert np.array_equal(np.take_along_axis(y, idx, axis=1), val)
+        assert len({tuple(r) for r in idx}) == 5 and all(len(set(r)) == k for r in idx)
+    am, _, _ = oracle.head_reduce(y)
+    assert np.array_equal(oracle.head_topk(y, 1)[0][:, 0], am)
+    assert oracle.head_topk(y, 12)[0][2, :10].tolist() == list(range(100, 110))
+
+
+def test_head_topk_selection_property_brute_force():
+    # every chosen row ranks above every row left out, under (value, then +0
+    # over -0, then smaller index), checked pair by pair on small rows
+    rng = np.random.default_rng(10)
+    for _ in range(50):
+        n = int(rng.integers(1, 12))
+        y = rng.integers(-3, 4, size=(1, n)).astype(np.float64)
+        y[0, rng.random(n) < 0.2] = -0.0
+        k = int(rng.integers(1, 14))
+        idx, val = oracle.head_topk(y, k)
+        chosen = [int(i) for i in idx[0] if i >= 0]
+        assert len(chosen) == min(k, n)
+
+        def above(a, b):
+            if y[0, a] != y[0, b]:
+                return y[0, a] > y[0, b]
+            if np.signbit(y[0, a]) != np.signbit(y[0, b]):
+                return not np.signbit(y[0, a])
+            return a < b
+        for p in range(len(chosen) - 1):
+            assert above(chosen[p], chosen[p + 1])
+        for a in chosen:
+            for b in set(range(n)) - set(chosen):
+                assert above(a, b)
+
+
 # ---------------------------------------------------------------- searched encoder
 def _exact_group(values, step_bits):
     """One 64-weight row group w = step * values (values integers), step an FP16
