@@ -278,12 +278,17 @@ __device__ void producer(const GemvArgs& a, uint8_t* smem, const Bars& bars, con
 // ------------------------------------------------------------------ x tile
 // MMA route: entry (g, tok, r) = 8 words = B fragments of the four 16-wide
 // K slices j of group g for lane r: word 2j = x[tok][16j+2r .. +1],
-// word 2j+1 = x[tok][16j+2r+8 .. +9] (bf16 pairs).
+// word 2j+1 = x[tok][16j+2r+8 .. +9] (bf16 pairs).  The entry's two halves
+// (slices 0-1, slices 2-3) sit in two planes, 16 bytes per entry each, the
+// second plane gc T 64 bytes after the first: a lane's 16-byte reads of one
+// plane are then consecutive across lanes (32-byte entries would make every
+// 16-byte read 2-way bank conflicted).
 __device__ inline void stage_x_bf16(const GemvArgs& a, uint8_t* smem, const Work& wk, int ctid,
                              int nthreads) {
   const int gc = wk.g_end - wk.g_begin;
   const int total = gc * a.T * 4;
   uint8_t* xs = smem + a.off_x;
+  const int hb = gc * a.T * 64;  // second plane
   for (int e = ctid; e < total; e += nthreads) {
     const int g = e / (a.T * 4);
     const int rem = e - g * a.T * 4;
@@ -297,7 +302,7 @@ __device__ inline void stage_x_bf16(const GemvArgs& a, uint8_t* smem, const Work
       uint2 o;
       o.x = w[r];
       o.y = w[4 + r];
-      *reinterpret_cast<uint2*>(xs + ((g * a.T + tok) * 4 + r) * 32 + 8 * j) = o;
+      *reinterpret_cast<uint2*>(xs + (j >> 1) * hb + ((g * a.T + tok) * 4 + r) * 16 + 8 * (j & 1)) = o;
     }
   }
 }
@@ -436,12 +441,12 @@ __device__ __forceinline__ void q8_pair_planes(const uint32_t (&w)[8], int p, ui
 // ------------------------------------------------------------------ per-group math
 // One group of one row tile on the MMA route: decode the lane's 32 codes, four
 // chained MMAs against the x fragments (the first starts from zero), scale,
-// accumulate.  xp[nb]: x fragments of token block nb for this lane (zeros if
-// the token is absent).
+// accumulate.  xp[nb]: x fragments of K slices 0-1 of token block nb for this
+// lane, xp[nb] + xh[nb] those of slices 2-3 (zeros if the token is absent).
 template <int BITS, int NT>
 __device__ __forceinline__ void mma_group(const uint8_t* blk, const uint8_t* sc,
-                                          const uint8_t* const (&xp)[NT], int lane, int q,
-                                          float (&acc)[NT][4]) {
+                                          const uint8_t* const (&xp)[NT], const int (&xh)[NT],
+                                          int lane, int q, float (&acc)[NT][4]) {
   uint32_t w[BITS];
   load_lane_words<BITS>(blk, lane, w);
   const __half2 sh = *reinterpret_cast<const __half2*>(sc + 4 * q);
@@ -449,7 +454,7 @@ __device__ __forceinline__ void mma_group(const uint8_t* blk, const uint8_t* sc,
 #pragma unroll
   for (int nb = 0; nb < NT; ++nb) {
     xa[nb] = *reinterpret_cast<const uint4*>(xp[nb]);
-    xb[nb] = *reinterpret_cast<const uint4*>(xp[nb] + 16);
+    xb[nb] = *reinterpret_cast<const uint4*>(xp[nb] + xh[nb]);
   }
   float d[NT][4], dh[NT][4];   // dh: high-nibble plane of 8-bit codes
 #pragma unroll
@@ -980,13 +985,15 @@ __device__ void consumer_xsmem(const GemvArgs& a, uint8_t* smem, const Bars& bar
   const uint8_t* ring = smem + a.off_ring;
   // MMA route: x fragments of token 8 nb + q, or the zero area if absent.
   const uint8_t* xbase[NT];
-  int xstep[NT];
+  int xstep[NT], xhalf[NT];
   if constexpr (ROUTE == kRouteMma) {
+    const int hb = (wk.g_end - wk.g_begin) * T * 64;  // second x plane (stage_x_bf16)
 #pragma unroll
     for (int nb = 0; nb < NT; ++nb) {
       const bool v = 8 * nb + q < T;
-      xbase[nb] = v ? smem + a.off_x + 1024 * nb + 32 * lane : smem + kZeroAreaOffset;
-      xstep[nb] = v ? T * 128 : 0;
+      xbase[nb] = v ? smem + a.off_x + 512 * nb + 16 * lane : smem + kZeroAreaOffset;
+      xstep[nb] = v ? T * 64 : 0;
+      xhalf[nb] = v ? hb : 16;   // the zero area holds 32 bytes
     }
   }
   const uint8_t* xf = smem + a.off_x + 64 * r;  // FMA route: entry (g, t, r) at (g T + t) 256 + 64 r
@@ -1014,7 +1021,8 @@ __device__ void consumer_xsmem(const GemvArgs& a, uint8_t* smem, const Bars& bar
           const uint8_t* xp[NT];
 #pragma unroll
           for (int nb = 0; nb < NT; ++nb) xp[nb] = xbase[nb] + (gx0 + gl) * xstep[nb];
-          mma_group<BITS, NT>(st + gl * kBlock, scb + gl * kScaleBytesPerBlock, xp, lane, q, acc);
+          mma_group<BITS, NT>(st + gl * kBlock, scb + gl * kScaleBytesPerBlock, xp, xhalf, lane, q,
+                              acc);
         } else {
           ffma_group<BITS, NT>(st + gl * kBlock, scb + gl * kScaleBytesPerBlock,
                                xf + (gx0 + gl) * T * 256, lane, q, T, facc);

@@ -297,12 +297,14 @@ int make_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, Plan
   const int cands[4] = {1, 2, 4, 8};
   bool have = false;
   Plan best;
-  // For T <= 8 the x-in-register kernel at the smallest K split (up to 4)
-  // that allows it beats every other candidate on GB300 -- measured on the
-  // 27B shapes (K = 5120: KS 1; K = 17408: KS 4, 7-15 % ahead of KS 1/2 with
-  // x in shared memory) -- because its consumers issue the fewest
-  // instructions per weight, and the split's per-job overhead grows with KS.
-  // Larger T, or no such candidate: the time model below decides.
+  // The x-in-register kernel at the smallest K split (up to 4) that allows
+  // it beats every other candidate on GB300 -- measured on the 27B shapes
+  // (T <= 8, K = 5120: KS 1; K = 17408: KS 4, 7-15 % ahead of KS 1/2 with x
+  // in shared memory; T = 12 and 16, K = 5120: KS 2, 205 / 213 us on the
+  // 248,320-row head against 230 / 372 us at KS 1 with x in shared memory) --
+  // because its consumers issue the fewest instructions per weight, and the
+  // split's per-job overhead grows with KS.  No such candidate: the time
+  // model below decides.
   bool have_xreg = false;
   Plan best_xreg;
   for (int ks : cands) {
@@ -333,7 +335,7 @@ int make_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, Plan
       best = p;
       have = true;
     }
-    if (!have_xreg && route == NQ_ROUTE_MMA && T <= 8 && ks <= 4 && p.func == xreg.func) {
+    if (!have_xreg && route == NQ_ROUTE_MMA && ks <= 4 && p.func == xreg.func) {
       best_xreg = p;
       have_xreg = true;
     }
