@@ -129,28 +129,19 @@ struct Plan {
   double est_us = 0;
 };
 
-// Shared-memory layout for a K-split and a stage size (64-groups per stage);
-// false if fewer than `min_stages` stages fit.
-bool layout_for(const Plan& base, int G, int T, int bits, int ks, int sg, int min_stages,
-                int smem_optin, int extra, Plan* out) {
+// Shared-memory layout for a K-split, a stage size (64-groups per stage) and a
+// number of partial-sum buffers; false if fewer than `min_stages` stages fit.
+bool layout_nbuf(const Plan& base, int G, int T, int bits, int ks, int sg, int min_stages,
+                 int smem_optin, int extra, int nbuf, Plan* out) {
   Plan p = base;
   p.ks = ks;
   p.sg = sg;
+  p.nbuf = nbuf;
   const int gc_max = (G + ks - 1) / ks;
   const bool x_in_regs = p.route == NQ_ROUTE_MMA && (p.ntok == kNtokXreg || p.ntok == kNtokXreg2);
   const long long x_bytes =
       x_in_regs ? 0 : 1LL * gc_max * T * (p.route == NQ_ROUTE_MMA ? 128 : 256);
-  // Partial-sum buffers in flight between the warps, the epilogue and the
-  // cluster's rank 0: deep for small T (cheap), shallow for large T.  The
-  // x-in-register kernels with one token block hand over two row tiles per
-  // buffer (JT = 2), so they need half as many buffers for the same slack.
-  // (a multiple of kEpiWarps: each buffer belongs to one epilogue warp)
   const int jt = (x_in_regs && p.ntok == kNtokXreg) ? 2 : 1;   // the kernel's kJobTiles
-  if (jt == 2) p.nbuf = T <= 2 ? 4 : 2;
-  else p.nbuf = T <= 2 ? kMaxBufs : T <= 4 ? 6 : T <= 8 ? 4 : 2;
-  static_assert(kMaxBufs % kEpiWarps == 0 && 6 % kEpiWarps == 0 && 4 % kEpiWarps == 0 &&
-                    2 % kEpiWarps == 0,
-                "buffer counts must be multiples of the epilogue warps");
   const int red_bytes = p.nbuf * kWarps * jt * 16 * T * 4;
   const int cl_bytes = ks > 1 ? p.nbuf * (ks - 1) * jt * 16 * T * 4 : 0;
   p.stage_bytes = align_up(sg * (block_bytes(bits) + kScaleBytesPerBlock), 128);
@@ -182,6 +173,40 @@ bool layout_for(const Plan& base, int G, int T, int bits, int ks, int sg, int mi
   }
   *out = p;
   return true;
+}
+
+// The layout with the deepest partial-sum buffering that still leaves three
+// ring stages, else the standard depth.  Buffers in flight between the warps,
+// the epilogue and the cluster's rank 0: deep for small T (cheap), shallower
+// for large T; the x-in-register kernels with one token block hand over two
+// row tiles per buffer (JT = 2), so they need half as many for the same
+// slack.  Measured on GB300 (27B shapes): one step deeper than standard is
+// 2-3 % faster at T = 8 and 16 where three stages remain (gate+up 23.1 ->
+// 22.6 us at T = 8, 33.5 -> 32.3 us at T = 16; down 17.4 -> 17.0 us at
+// T = 8; head 213.7 -> 206.7 us at T = 16), and slower where it costs the
+// third stage (the head at T = 8: 152 -> 160 us).  Counts are multiples of
+// kEpiWarps: each buffer belongs to one epilogue warp.
+bool layout_for(const Plan& base, int G, int T, int bits, int ks, int sg, int min_stages,
+                int smem_optin, int extra, Plan* out) {
+  const bool x_in_regs =
+      base.route == NQ_ROUTE_MMA && (base.ntok == kNtokXreg || base.ntok == kNtokXreg2);
+  const int jt = (x_in_regs && base.ntok == kNtokXreg) ? 2 : 1;
+  int std_nbuf, deep_nbuf;
+  if (jt == 2) {
+    std_nbuf = T <= 2 ? 4 : 2;
+    deep_nbuf = 4;
+  } else {
+    std_nbuf = T <= 2 ? kMaxBufs : T <= 4 ? 6 : T <= 8 ? 4 : 2;
+    deep_nbuf = T <= 8 ? std_nbuf : 6;
+  }
+  static_assert(kMaxBufs % kEpiWarps == 0 && 6 % kEpiWarps == 0 && 4 % kEpiWarps == 0 &&
+                    2 % kEpiWarps == 0,
+                "buffer counts must be multiples of the epilogue warps");
+  if (deep_nbuf > std_nbuf &&
+      layout_nbuf(base, G, T, bits, ks, sg, std::max(3, min_stages), smem_optin, extra, deep_nbuf,
+                  out))
+    return true;
+  return layout_nbuf(base, G, T, bits, ks, sg, min_stages, smem_optin, extra, std_nbuf, out);
 }
 
 int prepare_func(int dev, const void* func, int smem_optin) {
