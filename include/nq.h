@@ -34,18 +34,19 @@
  *   - Thread-safe: no state besides the per-device status word and cached
  *     per-device launch settings.
  *
- * PACKED LAYOUT (version 1)
+ * PACKED LAYOUT (version 2)
  * -------------------------
  *   Rows are taken in tiles of 16 (Nt = ceil(N/16) tiles; rows >= N of the
  *   last tile are padding with code 0 and scale +0), groups of 64 along K
  *   (G = K/64).  One "block" holds the codes of one row tile and one group,
  *   1024 codes, split among 32 lanes: lane L (q = L/4, r = L%4) owns 32 codes,
  *   16 pairs p = 4*j + i (j = 0..3 sixteen-wide K slices, i = 0..3):
- *       i = 0: row q,     k = 16j + 2r + {0, 1}
- *       i = 1: row q + 8, k = 16j + 2r + {0, 1}
- *       i = 2: row q,     k = 16j + 2r + 8 + {0, 1}
- *       i = 3: row q + 8, k = 16j + 2r + 8 + {0, 1}
- *   (k relative to the group).  Every code is stored biased, u = c + 2^(b-1),
+ *       i = 0: row q,     k = 16r + 4j + {0, 1}
+ *       i = 1: row q + 8, k = 16r + 4j + {0, 1}
+ *       i = 2: row q,     k = 16r + 4j + 2 + {0, 1}
+ *       i = 3: row q + 8, k = 16r + 4j + 2 + {0, 1}
+ *   (k relative to the group: the group's K order is permuted so that the
+ *   x values lane r multiplies, k = 16r .. 16r + 15, are contiguous).  Every code is stored biased, u = c + 2^(b-1),
  *   as an unsigned b-bit field.  The first code of a pair sits in the low
  *   16-bit half of a 32-bit word, the second at the same offset + 16.
  *   A lane's words (W = b 32-bit words) are:
@@ -284,7 +285,7 @@ int nq_selftest_wait_timeout(int limit_us, nq_stream_t stream);
 /* Static description of a status code. */
 const char* nq_status_string(int status);
 
-/* Packed-layout version implemented by this library (1). */
+/* Packed-layout version implemented by this library (2). */
 int nq_layout_version(void);
 
 #ifdef __cplusplus

@@ -33,7 +33,7 @@
 // slices are short (up to 5 groups per warp for T <= 8, 3 for T <= 16) each
 // consumer warp owns a fixed slice of those groups and keeps its x fragments
 // in registers ("x in registers"); otherwise the CTA's x slice sits in shared
-// memory, permuted into B-fragment order, and the warps take the groups of a
+// memory in B-fragment order, and the warps take the groups of a
 // stage in turn.  With x in registers, 4-bit codes take an fp16 route: x is
 // staged once as fp16 scaled by a power of two per token (exact, checked;
 // else the bf16 route), which lets the decode reach two nibbles per half
@@ -277,12 +277,13 @@ __device__ void producer(const GemvArgs& a, uint8_t* smem, const Bars& bars, con
 
 // ------------------------------------------------------------------ x tile
 // MMA route: entry (g, tok, r) = 8 words = B fragments of the four 16-wide
-// K slices j of group g for lane r: word 2j = x[tok][16j+2r .. +1],
-// word 2j+1 = x[tok][16j+2r+8 .. +9] (bf16 pairs).  The entry's two halves
-// (slices 0-1, slices 2-3) sit in two planes, 16 bytes per entry each, the
-// second plane gc T 64 bytes after the first: a lane's 16-byte reads of one
-// plane are then consecutive across lanes (32-byte entries would make every
-// 16-byte read 2-way bank conflicted).
+// K slices j of group g for lane r: words 2j, 2j + 1 = x[tok][16r + 4j ..
+// 16r + 4j + 3] (bf16 pairs, the layout's K order), i.e. the 32 bytes of x
+// at k = 16r .. 16r + 15 of the group.  The entry's two halves (slices 0-1,
+// slices 2-3) sit in two planes, 16 bytes per entry each, the second plane
+// gc T 64 bytes after the first: a lane's 16-byte reads of one plane are then
+// consecutive across lanes (32-byte entries would make every 16-byte read
+// 2-way bank conflicted).
 __device__ inline void stage_x_bf16(const GemvArgs& a, uint8_t* smem, const Work& wk, int ctid,
                              int nthreads) {
   const int gc = wk.g_end - wk.g_begin;
@@ -292,22 +293,17 @@ __device__ inline void stage_x_bf16(const GemvArgs& a, uint8_t* smem, const Work
   for (int e = ctid; e < total; e += nthreads) {
     const int g = e / (a.T * 4);
     const int rem = e - g * a.T * 4;
-    const int tok = rem >> 2, j = rem & 3;
-    const long long k0 = 64LL * (wk.g_begin + g) + 16 * j;
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<long long>(tok) * a.K + k0);
-    const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      uint2 o;
-      o.x = w[r];
-      o.y = w[4 + r];
-      *reinterpret_cast<uint2*>(xs + (j >> 1) * hb + ((g * a.T + tok) * 4 + r) * 16 + 8 * (j & 1)) = o;
-    }
+    const int tok = rem >> 2, r = rem & 3;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        a.x + static_cast<long long>(tok) * a.K + 64LL * (wk.g_begin + g) + 16 * r);
+    const int off = ((g * a.T + tok) * 4 + r) * 16;
+    *reinterpret_cast<uint4*>(xs + off) = __ldg(src);
+    *reinterpret_cast<uint4*>(xs + hb + off) = __ldg(src + 1);
   }
 }
 
-// FMA route: entry (g, tok, r) = 16 floats, [4j + m] = x[tok][16j + 2r + {0,1,8,9}[m]].
+// FMA route: entry (g, tok, r) = 16 floats, [4j + m] = x[tok][16r + 4j + m]
+// (the layout's K order: pair i of K slice j multiplies [4j + 2 (i / 2) + c]).
 __device__ inline void stage_x_f32(const GemvArgs& a, uint8_t* smem, const Work& wk, int ctid,
                             int nthreads) {
   const int gc = wk.g_end - wk.g_begin;
@@ -316,19 +312,20 @@ __device__ inline void stage_x_f32(const GemvArgs& a, uint8_t* smem, const Work&
   for (int e = ctid; e < total; e += nthreads) {
     const int g = e / (a.T * 4);
     const int rem = e - g * a.T * 4;
-    const int tok = rem >> 2, j = rem & 3;
-    const long long k0 = 64LL * (wk.g_begin + g) + 16 * j;
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<long long>(tok) * a.K + k0);
+    const int tok = rem >> 2, r = rem & 3;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        a.x + static_cast<long long>(tok) * a.K + 64LL * (wk.g_begin + g) + 16 * r);
     const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
     const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float4* dst = reinterpret_cast<float4*>(xs + ((g * a.T + tok) * 4 + r) * 64);
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int m = 0; m < 4; ++m) {
       float4 o;
-      o.x = __uint_as_float(w[r] << 16);
-      o.y = __uint_as_float(w[r] & 0xFFFF0000u);
-      o.z = __uint_as_float(w[4 + r] << 16);
-      o.w = __uint_as_float(w[4 + r] & 0xFFFF0000u);
-      *reinterpret_cast<float4*>(xs + ((g * a.T + tok) * 4 + r) * 64 + 16 * j) = o;
+      o.x = __uint_as_float(w[2 * m] << 16);
+      o.y = __uint_as_float(w[2 * m] & 0xFFFF0000u);
+      o.z = __uint_as_float(w[2 * m + 1] << 16);
+      o.w = __uint_as_float(w[2 * m + 1] & 0xFFFF0000u);
+      dst[m] = o;
     }
   }
 }
@@ -720,13 +717,12 @@ __device__ __forceinline__ void load_x_frags(const GemvArgs& a, const Slice& sl,
       for (int e = 0; e < 8; ++e) xr[i][nb][e] = 0u;
       const int tok = 8 * nb + q;
       if (i < n && tok < a.T) {
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(
-            a.x + static_cast<long long>(tok) * a.K + 64LL * (sl.gs + i) + 2 * r);
-#pragma unroll
-        for (int js = 0; js < 4; ++js) {
-          xr[i][nb][2 * js] = __ldg(src + 8 * js);
-          xr[i][nb][2 * js + 1] = __ldg(src + 8 * js + 4);
-        }
+        // the layout's K order: the lane's fragments are x at k = 16r .. 16r + 15
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.x + static_cast<long long>(tok) * a.K + 64LL * (sl.gs + i) + 16 * r);
+        const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+        xr[i][nb][0] = v0.x; xr[i][nb][1] = v0.y; xr[i][nb][2] = v0.z; xr[i][nb][3] = v0.w;
+        xr[i][nb][4] = v1.x; xr[i][nb][5] = v1.y; xr[i][nb][6] = v1.z; xr[i][nb][7] = v1.w;
       }
     }
   }
@@ -735,7 +731,8 @@ __device__ __forceinline__ void load_x_frags(const GemvArgs& a, const Slice& sl,
 // fp16 route of 4-bit codes (taken for T <= 2, where staging x costs less
 // than the shorter decode saves): the consumer warps stage the CTA's x range
 // once, as fp16 pairs of x * 2^e_t with one power of two e_t per token t, in
-// B-fragment order (the layout of stage_x_bf16) at off_xh.  e_t puts the
+// B-fragment order at off_xh (entry (g, t, r): 32 bytes, x at k = 16r ..
+// 16r + 15 of group g for token t; the layout's K order).  e_t puts the
 // token's largest |x| in [2^14, 2^15); every bf16 value then converts
 // exactly when none lies more than 31 binades below it (fp16 keeps 11
 // significant bits down to 2^-14 and steps of 2^-24 below), the maximum lies
@@ -809,10 +806,10 @@ __device__ inline bool stage_x_f16(const GemvArgs& a, uint8_t* smem, const Work&
 #pragma unroll
     for (int k = 0; k < 8; ++k)
       h[k] = cvt_f16x2(__uint_as_float(w[k] << 16) * sc, __uint_as_float(w[k] & 0xFFFF0000u) * sc);
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-      *reinterpret_cast<uint2*>(xs + ((g * T + tok) * 4 + r) * 32 + 8 * j) =
-          make_uint2(h[r], h[4 + r]);
+    // unit j (k = 16j .. 16j + 15) is lane j's whole fragment entry
+    uint4* dst = reinterpret_cast<uint4*>(xs + ((g * T + tok) * 4 + j) * 32);
+    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
   }
   asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
   return stat[32] == 0u;

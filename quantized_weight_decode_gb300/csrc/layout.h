@@ -1,4 +1,4 @@
-// Packed-code layout, version 1 (full description in include/nq.h).
+// Packed-code layout, version 2 (full description in include/nq.h).
 //
 // The groupwise encoding itself -- signed codes in 64-weight groups with one
 // FP16 scale each, w = scale * code -- is the one on the page "Qwen3.8-27B
@@ -6,8 +6,12 @@
 // artifact").  The page gives no storage layout; this one is ours, built for
 // the sm_103a kernels:
 //   * a row tile of 16 rows x one 64-group is one 1024-code block, split over
-//     the 32 lanes of a warp in exactly the order of the A operand of
-//     mma.m16n8k16 (lane q*4+r: rows q and q+8, k = 16j + 2r + {0,1,8,9});
+//     the 32 lanes of a warp in the register order of the A operand of
+//     mma.m16n8k16 (lane q*4+r: rows q and q+8), with the group's K order
+//     permuted so that the 16 k of lane r are k = 16r .. 16r + 15 (K slice j
+//     of the MMA takes k = 16r + 4j + {0,1} and 16r + 4j + 2 + {0,1}): a dot
+//     product does not depend on the order of its terms, and this one makes
+//     a lane's x fragments 32 contiguous bytes of x (two 16-byte loads);
 //   * the two codes of an A-fragment register sit at the same bit offset in
 //     the two 16-bit halves of a 32-bit word, so one mask-and-or turns them
 //     into two bf16 values 128 + u (u <= 127 fills the 7-bit mantissa of
@@ -34,7 +38,7 @@ constexpr int kTileRows = 16;           // rows per tile (MMA M)
 constexpr int kGroup = 64;              // codes per group along K
 constexpr int kLanes = 32;
 constexpr int kScaleBytesPerBlock = 32; // 16 FP16 scales
-constexpr int kLayoutVersion = 1;
+constexpr int kLayoutVersion = 2;
 
 NQ_HD int block_bytes(int bits) { return 128 * bits; }   // 32 lanes * bits words * 4 B
 
@@ -44,7 +48,7 @@ NQ_HD void lane_code_coords(int lane, int p, int h, int* row, int* k) {
   const int q = lane >> 2, r = lane & 3;
   const int j = p >> 2, i = p & 3;
   *row = q + 8 * (i & 1);
-  *k = 16 * j + 2 * r + 8 * (i >> 1) + h;
+  *k = 16 * r + 4 * j + 2 * (i >> 1) + h;
 }
 
 // Byte offset, inside a block, of word w of lane `lane`.

@@ -29,7 +29,7 @@ def test_exports_every_header_symbol():
     for name in sorted(declared):
         assert hasattr(lib, name), name
     assert declared == set(nqp.EXPORTED)
-    assert nqp.layout_version() == 1
+    assert nqp.layout_version() == 2
 
 
 @pytest.mark.parametrize("bits", [4, 5, 6, 8])
@@ -85,7 +85,7 @@ def test_pack_matches_header_spec(bits):
                     j, i = p // 4, p % 4
                     for h in range(2):
                         row = q + 8 * (i % 2)
-                        k = 16 * j + 2 * r + 8 * (i // 2) + h
+                        k = 16 * r + 4 * j + 2 * (i // 2) + h
                         n = rt * 16 + row
                         u_expect = (int(codes[n, g * 64 + k]) if n < N else 0) + bias
                         u = 0
