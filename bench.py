@@ -564,9 +564,12 @@ def run_ours(args, rank, world, local_rank):
     dom = kernels["gate_up_T1"]
     roofline = {"bound": "hbm", "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
                 "frac": round(dom["gbs"] / peak, 4), "traffic": stored_traffic(),
-                "kernel": "gemv_kernel<4,MMA,1> gate+up Q4 K=5120 N=34816 T=1",
+                "kernel": "gemv_kernel<4,1,3> (4-bit, MMA route, x in registers) "
+                          "gate+up Q4 K=5120 N=34816 at T=1",
                 "bytes_per_launch": packed_bytes(4, HIDDEN, 2 * INTER),
-                "peak_source": peak_kind}
+                "peak_source": peak_kind,
+                # the same product at every T of the step (T=16: gemv_kernel<4,1,4>)
+                "frac_by_T": {str(T): kernels[f"gate_up_T{T}"]["frac"] for T in TS}}
     cpu_v, _, cpu_s, cpu_desc = oracle_sample(args.cpu_seconds)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": steps,
