@@ -194,11 +194,12 @@ bool layout_for(const Plan& base, int G, int T, int bits, int ks, int sg, int mi
   int std_nbuf, deep_nbuf;
   if (jt == 2) {
     std_nbuf = T <= 2 ? 4 : 2;
-    // T = 1: eight pair buffers hold a whole CTA's share of the 34,816-row
-    // gate+up product, so its consumers never wait for the epilogue: 19.1 ->
-    // 18.7 us there even at one ring stage less (no gain at T = 2 or on the
-    // K-split down projection).
-    deep_nbuf = T == 1 ? kMaxBufs : 4;
+    // T <= 4: eight pair buffers (at T = 1 a whole CTA's share of the
+    // 34,816-row gate+up product), so the consumers hardly ever wait for the
+    // epilogue: gate+up 19.1 -> 18.7 us at T = 1 and 20.1 -> 19.8 us at T = 4,
+    // down 15.1 -> 14.8 us at T = 4, even at one ring stage less; the same at
+    // T = 2 within noise; the head keeps its third stage (and its depth).
+    deep_nbuf = T <= 4 ? kMaxBufs : 4;
   } else {
     std_nbuf = T <= 2 ? kMaxBufs : T <= 4 ? 6 : T <= 8 ? 4 : 2;
     deep_nbuf = T <= 8 ? std_nbuf : 6;
