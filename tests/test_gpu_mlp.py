@@ -66,7 +66,7 @@ def _check_act(act_bits, cg, sg, cu, su, xb):
     return ref, tol
 
 
-@pytest.mark.parametrize("bits,T", [(4, 1), (4, 2), (4, 8), (5, 3), (6, 16)])
+@pytest.mark.parametrize("bits,T", [(4, 1), (4, 2), (4, 8), (5, 3), (6, 16), (8, 4)])
 def test_swiglu_product(bits, T):
     I, H = 1000 // 8 * 8, 1024
     cg, sg, cu, su, xb, packed, sp = _gate_up_case((700, bits, T), bits, I, H, T)
@@ -111,6 +111,12 @@ def _check_layer(I, H, Hout, bits_gu, bits_down, T, tag):
 @pytest.mark.parametrize("T", [1, 4, 8])
 def test_mlp_layer(T):
     _check_layer(I=1024, H=512, Hout=384, bits_gu=4, bits_down=5, T=T, tag=(702, T))
+
+
+@pytest.mark.parametrize("bits_gu,bits_down,T", [(8, 8, 2), (6, 4, 16)])
+def test_mlp_layer_other_widths(bits_gu, bits_down, T):
+    _check_layer(I=1024, H=512, Hout=384, bits_gu=bits_gu, bits_down=bits_down, T=T,
+                 tag=(704, bits_gu, bits_down, T))
 
 
 @pytest.mark.slow
