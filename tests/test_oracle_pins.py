@@ -183,7 +183,8 @@ def test_dequant_matches_rationals_sample():
 
 
 # ---------------------------------------------------------------- product
-@pytest.mark.parametrize("bits,k,n,t", [(4, 64, 3, 1), (5, 128, 4, 2), (6, 256, 8, 4), (6, 192, 5, 3)])
+@pytest.mark.parametrize("bits,k,n,t", [(4, 64, 3, 1), (5, 128, 4, 2), (6, 256, 8, 4), (6, 192, 5, 3),
+                                         (8, 128, 4, 2)])
 def test_gemv_against_exact_rationals(bits, k, n, t):
     rng = synth.generator(0, 104, bits, k)
     codes = synth.uniform_codes(rng, n, k, bits)
