@@ -252,18 +252,35 @@ def _planted(codes, sb, xb, kind):
     elif kind == "tokens_swapped":
         w = np.repeat(s, 64, axis=1) * c
         return oracle.bf16_to_f64(xb[::-1]) @ w.T
+    elif kind == "high_plane_factor":
+        # an 8-bit code taken as hi * 16 + lo with the high nibble weighed 15
+        u = codes.astype(np.int64) + 128
+        w = np.repeat(s, 64, axis=1) * (15 * ((u >> 4) - 8) + (u & 15))
+    elif kind == "k_order_of_other_layout":
+        # x read in the K order k = 16j + 2r + 8h + c instead of 16r + 4j + 2h + c
+        perm = np.empty(64, dtype=np.int64)
+        for j in range(4):
+            for r in range(4):
+                for h in range(2):
+                    for cc in range(2):
+                        perm[16 * r + 4 * j + 2 * h + cc] = 16 * j + 2 * r + 8 * h + cc
+        full = (np.arange(k) // 64) * 64 + perm[np.arange(k) % 64]
+        w = np.repeat(s, 64, axis=1) * c[:, full]
     else:
         raise ValueError(kind)
     return oracle.bf16_to_f64(xb) @ w.T
 
 
-@pytest.mark.parametrize("kind", ["group_off_by_one", "scale_sign_dropped", "code_bias",
-                                  "k_pairs_swapped", "tokens_swapped"])
-def test_tolerance_catches_planted_mistakes(kind):
-    rng = synth.generator(0, 106)
+@pytest.mark.parametrize("bits,kind", [(5, "group_off_by_one"), (5, "scale_sign_dropped"),
+                                       (5, "code_bias"), (5, "k_pairs_swapped"),
+                                       (5, "tokens_swapped"), (8, "high_plane_factor"),
+                                       (5, "k_order_of_other_layout"),
+                                       (8, "k_order_of_other_layout")])
+def test_tolerance_catches_planted_mistakes(bits, kind):
+    rng = synth.generator(0, 106, bits)
     n, k, t = 32, 1024, 2
-    codes = synth.uniform_codes(rng, n, k, 5)
-    sb = oracle.rtn_scales(synth.gauss_weights(rng, n, k), 15)
+    codes = synth.uniform_codes(rng, n, k, bits)
+    sb = oracle.rtn_scales(synth.gauss_weights(rng, n, k), oracle.QMAX[bits])
     sb = sb ^ (synth.sign_flips(rng, n, k // 64).astype(np.uint16) << 15)
     xb = synth.gauss_x_bf16(rng, t, k, outliers=synth.outlier_channels(rng, k))
     y, e = oracle.gemv(codes, sb, xb)
