@@ -60,3 +60,25 @@ def device_weight(nqp, torch, case, dev):
 
 def device_x(torch, case, dev):
     return torch.from_numpy(case["xb"].view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+# Fused head (argmax / maximum / logsumexp) against the kernel's own logits:
+# argmax and maximum exact, logsumexp within 4e-5 + 1e-6 |lse| of the fp64
+# logsumexp of those logits (fp32 running sums, merged in a fixed order).
+LSE_ABS, LSE_REL = 4e-5, 1e-6
+
+
+def lse64(y):
+    y = y.astype(np.float64)
+    m = y.max(axis=1)
+    return m + np.log(np.exp(y - m[:, None]).sum(axis=1))
+
+
+def head_check_self(y, am, mx, lse):
+    """argmax / max / lse against the kernel's own logits."""
+    T = y.shape[0]
+    ref_am = np.argmax(y, axis=1)
+    assert np.array_equal(am, ref_am), (am, ref_am)
+    assert np.array_equal(mx.view(np.uint32), y[np.arange(T), am].view(np.uint32))
+    ref = lse64(y)
+    assert np.all(np.abs(lse - ref) <= LSE_ABS + LSE_REL * np.abs(ref)), (lse, ref)

@@ -15,11 +15,11 @@ import torch
 
 import oracle
 import quantized_weight_decode_gb300 as nqp
-from cases import device_weight, device_x, oracle_inputs, rtn_case, uniform_case
+from cases import (LSE_ABS, LSE_REL, device_weight, device_x, head_check_self, oracle_inputs,
+                   rtn_case, uniform_case)
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
-LSE_ABS, LSE_REL = 4e-5, 1e-6
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -30,12 +30,6 @@ def built():
     assert nqp.last_device_error() == 0
 
 
-def _lse64(y):
-    y = y.astype(np.float64)
-    m = y.max(axis=1)
-    return m + np.log(np.exp(y - m[:, None]).sum(axis=1))
-
-
 def _head(case, packed, sp, store_y=True, ws=None):
     T, K, N, bits = case["T"], case["K"], case["N"], case["bits"]
     x = device_x(torch, case, DEV)[:T].contiguous()
@@ -43,16 +37,6 @@ def _head(case, packed, sp, store_y=True, ws=None):
     am, mx, lse = nqp.gemv_head(packed, sp, x, K, N, T, bits, y=y, workspace=ws)
     assert nqp.last_device_error() == 0
     return (None if y is None else y.cpu().numpy()), am.cpu().numpy(), mx.cpu().numpy(), lse.cpu().numpy()
-
-
-def _check_self(y, am, mx, lse):
-    """argmax / max / lse against the kernel's own logits."""
-    T = y.shape[0]
-    ref_am = np.argmax(y, axis=1)
-    assert np.array_equal(am, ref_am), (am, ref_am)
-    assert np.array_equal(mx.view(np.uint32), y[np.arange(T), am].view(np.uint32))
-    ref = _lse64(y)
-    assert np.all(np.abs(lse - ref) <= LSE_ABS + LSE_REL * np.abs(ref)), (lse, ref)
 
 
 def _check_oracle(case, am, mx, lse, rows=None):
@@ -85,7 +69,7 @@ def test_head_matches_gemv_and_oracle(T):
         y2 = torch.full((T, N), float("nan"), dtype=torch.float32, device=DEV)
         nqp.gemv(packed, sp, x, y2, K, N, T, bits)
         assert np.array_equal(y.view(np.uint32), y2.cpu().numpy().view(np.uint32))
-        _check_self(y, am, mx, lse)
+        head_check_self(y, am, mx, lse)
         _check_oracle(case, am, mx, lse)
 
 
@@ -99,7 +83,7 @@ def test_head_without_logits_and_repeat_calls():
         assert np.array_equal(am, am2)
         assert np.array_equal(mx.view(np.uint32), mx2.view(np.uint32))
         assert np.array_equal(lse.view(np.uint32), lse2.view(np.uint32))
-    _check_self(y, am, mx, lse)
+    head_check_self(y, am, mx, lse)
 
 
 def test_head_ties_go_to_the_smallest_row():
@@ -150,7 +134,7 @@ def test_head_full_size(T):
     case = rtn_case((504, T), bits, N, K, T)
     packed, sp = device_weight(nqp, torch, case, DEV)
     y, am, mx, lse = _head(case, packed, sp)
-    _check_self(y, am, mx, lse)
+    head_check_self(y, am, mx, lse)
     rng = np.random.default_rng(3)
     rows = np.unique(np.concatenate([am, rng.choice(N, 256, replace=False)]))
     codes, sb = oracle_inputs(case, rows)
@@ -167,7 +151,7 @@ def test_head_proposal_head_shape(bits, T):
     case = rtn_case((505, bits, T), bits, N, K, T)
     packed, sp = device_weight(nqp, torch, case, DEV)
     y, am, mx, lse = _head(case, packed, sp)
-    _check_self(y, am, mx, lse)
+    head_check_self(y, am, mx, lse)
     rng = np.random.default_rng(4)
     rows = np.unique(np.concatenate([am, rng.choice(N, 256, replace=False)]))
     codes, sb = oracle_inputs(case, rows)

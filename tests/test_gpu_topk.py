@@ -13,8 +13,7 @@ import torch
 
 import oracle
 import quantized_weight_decode_gb300 as nqp
-from cases import device_weight, device_x, oracle_inputs, rtn_case, uniform_case
-from test_gpu_head import _check_self as head_check_self
+from cases import device_weight, device_x, head_check_self, oracle_inputs, rtn_case, uniform_case
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0") if torch.cuda.is_available() else None

@@ -10,11 +10,10 @@ import pytest
 import torch
 
 import quantized_weight_decode_gb300 as nqp
-from cases import device_weight, device_x, rtn_case, uniform_case
+from cases import LSE_ABS, LSE_REL, device_weight, device_x, rtn_case, uniform_case
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
-LSE_ABS, LSE_REL = 4e-5, 1e-6   # the logsumexp tolerance of the fused-head tests
 
 
 @pytest.fixture(scope="module", autouse=True)
