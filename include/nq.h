@@ -105,7 +105,10 @@ typedef enum {
 } nq_route;
 
 /* Byte sizes of the packed codes and packed scales of a W[N, K] tensor.
- * K % 64 == 0, K > 0, N > 0, bits in {4, 5, 6, 8}; outputs are host pointers. */
+ * K % 64 == 0, K > 0, N > 0, bits in {4, 5, 6, 8}; outputs are host pointers.
+ * Every entry point rejects K / 64 > 2^30 or more than 2^31 - 1 row tiles
+ * (N > 16 (2^31 - 1)) with NQ_EINVAL: the kernels index groups and row tiles
+ * with 32-bit integers. */
 int nq_packed_bytes(int64_t K, int64_t N, int bits, size_t* codes_bytes, size_t* scales_bytes);
 
 /* Host packer.  codes: host int8 [N, K] row-major, values in the signed range
@@ -115,6 +118,17 @@ int nq_packed_bytes(int64_t K, int64_t N, int bits, size_t* codes_bytes, size_t*
  * non-finite scale (nothing is written in that case). */
 int nq_pack(const int8_t* codes, const uint16_t* scales, int64_t K, int64_t N, int bits,
             void* packed_out, uint16_t* scales_out);
+
+/* Host packer of a gate+up matrix for nq_gemv_swiglu / nq_mlp: gate and up
+ * (host int8 codes [I, K] and host FP16 scale bits [I, K/64] each, row-major)
+ * packed as one matrix of N = 2 I rows interleaved per 8 -- packed row
+ * 16 r + m is gate row 8 r + m and packed row 16 r + 8 + m is up row 8 r + m
+ * (m < 8) -- so that a C caller needs no row permutation of its own.  I must
+ * be a multiple of 8 (NQ_EINVAL); outputs as nq_pack with N = 2 I.  Same
+ * range checks as nq_pack (NQ_ERANGE, nothing written). */
+int nq_pack_gate_up(const int8_t* codes_gate, const uint16_t* scales_gate, const int8_t* codes_up,
+                    const uint16_t* scales_up, int64_t K, int64_t I, int bits, void* packed_out,
+                    uint16_t* scales_out);
 
 /* Host inverse of nq_pack (test and inspection aid).  All pointers host. */
 int nq_unpack(const void* packed, const uint16_t* scales_packed, int64_t K, int64_t N, int bits,
@@ -258,7 +272,10 @@ int nq_head_topk_workspace_bytes(size_t* bytes);
  * part that must start at zero (the arrival counter) on its stream before
  * launching.  Calls that overlap on the GPU (other streams, other host
  * threads without ordering) race on the array and give wrong results: order
- * them on one stream. */
+ * them on one stream.  The looked-up address stays cached for the life of
+ * the process: after cudaDeviceReset (or anything else that destroys the
+ * device's primary context) the library must be unloaded and loaded again,
+ * or the process restarted, before this entry point is used on that device. */
 #define NQ_HEAD_SCRATCH_BYTES 139520
 int nq_gemv_head_noalloc(const void* packed, const uint16_t* scales, const void* x_bf16, float* y,
                          int64_t K, int64_t N, int T, int bits, int32_t* argmax, float* maxval,

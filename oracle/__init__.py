@@ -46,7 +46,7 @@ import numpy as np
 __all__ = [
     "QMAX", "GROUP", "fp16_to_f64", "bf16_to_f64", "f64_to_fp16_bits",
     "rtn_scales", "rtn_encode", "dequant", "dequant_f32", "gemv",
-    "gemv_rows", "tolerance_ok", "max_violation",
+    "tolerance_ok", "max_violation",
 ]
 
 GROUP = 64                       # weights per group along K
@@ -277,11 +277,6 @@ def gemv(codes: np.ndarray, scale_bits: np.ndarray, x_bits: np.ndarray):
     return y, e
 
 
-def gemv_rows(codes_rows: np.ndarray, scale_rows: np.ndarray, x_bits: np.ndarray):
-    """Same as gemv, for a subset of output rows given by their codes/scales."""
-    return gemv(codes_rows, scale_rows, x_bits)
-
-
 # --------------------------------------------------------------------------
 # Verify-head reductions over the outputs of one token (page "giveen/ninfer-ext",
 # section "Engineering": single-pass logsumexp; page "Qwen3.8-27B for NInfer on
@@ -295,7 +290,11 @@ def head_reduce(y):
     y = np.asarray(y, dtype=np.float64)
     am = np.argmax(y, axis=1)                       # first occurrence of the maximum
     m = y[np.arange(y.shape[0]), am]
-    lse = m + np.log(np.sum(np.exp(y - m[:, None]), axis=1))
+    # a +inf logit makes the sum +inf; the shifted form would compute inf - inf
+    fin = np.where(np.isposinf(m), 0.0, m)
+    with np.errstate(invalid="ignore"):
+        lse = fin + np.log(np.sum(np.exp(y - fin[:, None]), axis=1))
+    lse = np.where(np.isposinf(m), np.inf, lse)
     return am, m, lse
 
 

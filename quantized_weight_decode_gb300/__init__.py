@@ -19,7 +19,7 @@ import numpy as np
 
 __all__ = [
     "NQError", "ROUTE_AUTO", "ROUTE_MMA", "ROUTE_FFMA", "lib", "lib_path", "build",
-    "packed_bytes", "pack", "unpack", "pack_device", "quantize_rtn", "quantize_search", "gemv", "gemv_swiglu", "mlp", "interleave_gate_up", "gemv_head",
+    "packed_bytes", "pack", "pack_gate_up", "unpack", "pack_device", "quantize_rtn", "quantize_search", "gemv", "gemv_swiglu", "mlp", "interleave_gate_up", "gemv_head",
     "head_workspace_bytes", "gemv_head_noalloc", "gemv_head_topk", "head_topk_workspace_bytes",
     "dequant",
     "last_device_error", "plan", "selftest_wait_timeout", "status_string", "layout_version",
@@ -40,6 +40,7 @@ _ip = ctypes.POINTER(ctypes.c_int)
 _SIGS = {
     "nq_packed_bytes": (_i32, [_i64, _i64, _i32, _szp, _szp]),
     "nq_pack": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _vp]),
+    "nq_pack_gate_up": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp]),
     "nq_unpack": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _vp]),
     "nq_pack_device": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp]),
     "nq_quantize_rtn": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _vp]),
@@ -146,6 +147,24 @@ def pack(codes: np.ndarray, scales: np.ndarray, bits: int) -> tuple[np.ndarray, 
     sout = np.empty(sb // 2, dtype=np.uint16)
     _check(lib().nq_pack(codes.ctypes.data, scales.ctypes.data, K, N, bits,
                          out.ctypes.data, sout.ctypes.data), "nq_pack")
+    return out, sout
+
+
+def pack_gate_up(codes_gate: np.ndarray, scales_gate: np.ndarray, codes_up: np.ndarray,
+                 scales_up: np.ndarray, bits: int) -> tuple[np.ndarray, np.ndarray]:
+    """Host packer of a gate+up matrix in nq_gemv_swiglu's row order
+    (nq_pack_gate_up): gate and up int8 codes [I, K], FP16 scale bits
+    [I, K/64] -> packed codes and scales of the [2 I, K] matrix."""
+    cg = np.ascontiguousarray(codes_gate, dtype=np.int8)
+    cu = np.ascontiguousarray(codes_up, dtype=np.int8)
+    sg = np.ascontiguousarray(scales_gate).view(np.uint16)
+    su = np.ascontiguousarray(scales_up).view(np.uint16)
+    I, K = cg.shape
+    cb, sb = packed_bytes(K, 2 * I, bits)
+    out = np.empty(cb, dtype=np.uint8)
+    sout = np.empty(sb // 2, dtype=np.uint16)
+    _check(lib().nq_pack_gate_up(cg.ctypes.data, sg.ctypes.data, cu.ctypes.data, su.ctypes.data,
+                                 K, I, bits, out.ctypes.data, sout.ctypes.data), "nq_pack_gate_up")
     return out, sout
 
 

@@ -27,7 +27,7 @@ int* device_status_ptr() {
 // row-major code matrix and writes its words; lanes 0..15 also write the
 // scale of row `lane` of the tile.
 template <int BITS>
-__global__ void pack_kernel(const int8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
+__global__ void nq_pack_kernel(const int8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
                             long long K, long long N, int G, long long nthreads,
                             uint8_t* __restrict__ packed, uint16_t* __restrict__ scales_out) {
   const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
@@ -71,10 +71,10 @@ cudaError_t launch_pack_device(const int8_t* codes, const uint16_t* scales, long
   const long long grid = (nthreads + block - 1) / block;
   auto* out = static_cast<uint8_t*>(packed);
   switch (bits) {
-    case 4: pack_kernel<4><<<grid, block, 0, st>>>(codes, scales, K, N, G, nthreads, out, scales_out); break;
-    case 5: pack_kernel<5><<<grid, block, 0, st>>>(codes, scales, K, N, G, nthreads, out, scales_out); break;
-    case 8: pack_kernel<8><<<grid, block, 0, st>>>(codes, scales, K, N, G, nthreads, out, scales_out); break;
-    default: pack_kernel<6><<<grid, block, 0, st>>>(codes, scales, K, N, G, nthreads, out, scales_out); break;
+    case 4: nq_pack_kernel<4><<<grid, block, 0, st>>>(codes, scales, K, N, G, nthreads, out, scales_out); break;
+    case 5: nq_pack_kernel<5><<<grid, block, 0, st>>>(codes, scales, K, N, G, nthreads, out, scales_out); break;
+    case 8: nq_pack_kernel<8><<<grid, block, 0, st>>>(codes, scales, K, N, G, nthreads, out, scales_out); break;
+    default: nq_pack_kernel<6><<<grid, block, 0, st>>>(codes, scales, K, N, G, nthreads, out, scales_out); break;
   }
   return cudaGetLastError();
 }
@@ -82,7 +82,7 @@ cudaError_t launch_pack_device(const int8_t* codes, const uint16_t* scales, long
 // ------------------------------------------------------------------ dequant
 // w = fp32(scale) * fp32(code), exact; uses the GEMV's own decode of a lane.
 template <int BITS>
-__global__ void dequant_kernel(const uint8_t* __restrict__ packed,
+__global__ void nq_dequant_kernel(const uint8_t* __restrict__ packed,
                                const uint16_t* __restrict__ scales, long long K, long long N,
                                int G, long long nthreads, float* __restrict__ w) {
   const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
@@ -128,10 +128,10 @@ cudaError_t launch_dequant(const void* packed, const uint16_t* scales, float* w,
   const long long grid = (nthreads + block - 1) / block;
   auto* in = static_cast<const uint8_t*>(packed);
   switch (bits) {
-    case 4: dequant_kernel<4><<<grid, block, 0, st>>>(in, scales, K, N, G, nthreads, w); break;
-    case 5: dequant_kernel<5><<<grid, block, 0, st>>>(in, scales, K, N, G, nthreads, w); break;
-    case 8: dequant_kernel<8><<<grid, block, 0, st>>>(in, scales, K, N, G, nthreads, w); break;
-    default: dequant_kernel<6><<<grid, block, 0, st>>>(in, scales, K, N, G, nthreads, w); break;
+    case 4: nq_dequant_kernel<4><<<grid, block, 0, st>>>(in, scales, K, N, G, nthreads, w); break;
+    case 5: nq_dequant_kernel<5><<<grid, block, 0, st>>>(in, scales, K, N, G, nthreads, w); break;
+    case 8: nq_dequant_kernel<8><<<grid, block, 0, st>>>(in, scales, K, N, G, nthreads, w); break;
+    default: nq_dequant_kernel<6><<<grid, block, 0, st>>>(in, scales, K, N, G, nthreads, w); break;
   }
   return cudaGetLastError();
 }
@@ -140,7 +140,7 @@ cudaError_t launch_dequant(const void* packed, const uint16_t* scales, float* w,
 // One warp per 64-group: absmax by warp reduction (exact), scale = FP16
 // round-to-nearest-even of the fp64 quotient absmax / qmax, codes
 // = clamp(rint(w / s)) with the quotient in fp64 (IEEE, correctly rounded).
-__global__ void quantize_rtn_kernel(const float* __restrict__ w, long long K, long long ngroups,
+__global__ void nq_quantize_rtn_kernel(const float* __restrict__ w, long long K, long long ngroups,
                                     int G, int bits, int8_t* __restrict__ codes,
                                     uint16_t* __restrict__ scales, int* status) {
   const long long gw = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
@@ -179,7 +179,7 @@ cudaError_t launch_quantize_rtn(const float* w, long long K, long long N, int bi
   const long long ngroups = N * G;
   const int block = 256;  // 8 groups per block
   const long long grid = (ngroups * 32 + block - 1) / block;
-  quantize_rtn_kernel<<<grid, block, 0, st>>>(w, K, ngroups, G, bits, codes, scales, status);
+  nq_quantize_rtn_kernel<<<grid, block, 0, st>>>(w, K, ngroups, G, bits, codes, scales, status);
   return cudaGetLastError();
 }
 
@@ -197,7 +197,7 @@ cudaError_t launch_quantize_rtn(const float* w, long long K, long long N, int bi
 // candidate; candidates whose scale overflows FP16 take no part (if all do,
 // NQ_ERANGE).  One warp per group: lane l holds weights 2l, 2l + 1 and
 // candidates l and l + 32.
-__global__ void quantize_search_kernel(const float* __restrict__ w, const float* __restrict__ imp,
+__global__ void nq_quantize_search_kernel(const float* __restrict__ w, const float* __restrict__ imp,
                                        long long K, long long ngroups, int G, int bits,
                                        int8_t* __restrict__ codes, uint16_t* __restrict__ scales,
                                        int* status) {
@@ -280,7 +280,7 @@ cudaError_t launch_quantize_search(const float* w, const float* imatrix, long lo
   const long long ngroups = N * G;
   const int block = 256;  // 8 groups per block
   const long long grid = (ngroups * 32 + block - 1) / block;
-  quantize_search_kernel<<<grid, block, 0, st>>>(w, imatrix, K, ngroups, G, bits, codes, scales,
+  nq_quantize_search_kernel<<<grid, block, 0, st>>>(w, imatrix, K, ngroups, G, bits, codes, scales,
                                                  status);
   return cudaGetLastError();
 }
@@ -288,7 +288,7 @@ cudaError_t launch_quantize_search(const float* w, const float* imatrix, long lo
 // ------------------------------------------------------------------ self-test
 // Waits on a barrier that nothing completes; the bounded wait gives up after
 // `limit_ns`, records NQ_ETIMEOUT and the kernel returns normally.
-__global__ void selftest_timeout_kernel(unsigned long long limit_ns, int* status) {
+__global__ void nq_selftest_timeout_kernel(unsigned long long limit_ns, int* status) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
   if (threadIdx.x != 0) return;
@@ -300,7 +300,7 @@ __global__ void selftest_timeout_kernel(unsigned long long limit_ns, int* status
 }
 
 cudaError_t launch_selftest_timeout(unsigned long long limit_ns, int* status, cudaStream_t st) {
-  selftest_timeout_kernel<<<1, 32, 0, st>>>(limit_ns, status);
+  nq_selftest_timeout_kernel<<<1, 32, 0, st>>>(limit_ns, status);
   return cudaGetLastError();
 }
 

@@ -1098,7 +1098,11 @@ __device__ __forceinline__ void head_push(float& m, float& s, int& a, float v, i
     s = s * __expf(m - v) + 1.f;
     m = v;
     a = idx;
-  } else if (v != -INFINITY) {
+  } else if (v == -INFINITY) {
+    // contributes exp(-inf) = 0 (and leaves an empty state empty)
+  } else if (v == m) {
+    s += 1.f;  // exp(0); also keeps a second +inf logit from forming inf - inf
+  } else {
     s += __expf(v - m);
   }
 }
@@ -1110,7 +1114,10 @@ __device__ __forceinline__ void head_merge(float& m, float& s, int& a, float mo,
     a = ao;
     return;
   }
-  if (mo > m || (mo == m && ao < a)) {
+  if (mo == m) {  // equal maxima (both +inf included): the factor is exactly 1
+    s = s + so;
+    a = min(a, ao);
+  } else if (mo > m) {
     s = s * __expf(m - mo) + so;
     m = mo;
     a = ao;
@@ -1434,7 +1441,7 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
 
 // ------------------------------------------------------------------ kernel
 template <int BITS, int ROUTE, int NTOK>
-__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) nq_gemv_kernel(const __grid_constant__ GemvArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Bars bars{smem_addr(smem)};

@@ -5,12 +5,12 @@ namespace nq {
 
 const void* gemv_kernel_q6(int route, int ntok) {
   if (route == kRouteMma) {
-    if (ntok == kNtokXreg) return reinterpret_cast<const void*>(&gemv_kernel<6, kRouteMma, kNtokXreg>);
-    if (ntok == kNtokXreg2) return reinterpret_cast<const void*>(&gemv_kernel<6, kRouteMma, kNtokXreg2>);
-    return ntok == 1 ? reinterpret_cast<const void*>(&gemv_kernel<6, kRouteMma, 1>)
-                     : reinterpret_cast<const void*>(&gemv_kernel<6, kRouteMma, 2>);
+    if (ntok == kNtokXreg) return reinterpret_cast<const void*>(&nq_gemv_kernel<6, kRouteMma, kNtokXreg>);
+    if (ntok == kNtokXreg2) return reinterpret_cast<const void*>(&nq_gemv_kernel<6, kRouteMma, kNtokXreg2>);
+    return ntok == 1 ? reinterpret_cast<const void*>(&nq_gemv_kernel<6, kRouteMma, 1>)
+                     : reinterpret_cast<const void*>(&nq_gemv_kernel<6, kRouteMma, 2>);
   }
-  return reinterpret_cast<const void*>(&gemv_kernel<6, kRouteFfma, 4>);
+  return reinterpret_cast<const void*>(&nq_gemv_kernel<6, kRouteFfma, 4>);
 }
 
 }  // namespace nq

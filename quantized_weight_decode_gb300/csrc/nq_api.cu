@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <climits>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -89,7 +90,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int check_shape(int64_t K, int64_t N, int bits) {
   if (K <= 0 || N <= 0 || K % kGroup != 0) return NQ_EINVAL;
   if (bits < 4 || bits > 8 || bits == 7) return NQ_EINVAL;
-  if (K / kGroup > (1LL << 30) || N > (1LL << 40)) return NQ_EINVAL;
+  // The kernels index groups and row tiles with 32-bit integers.
+  if (K / kGroup > (1LL << 30) || (N + kTileRows - 1) / kTileRows > INT_MAX) return NQ_EINVAL;
   return NQ_OK;
 }
 
@@ -454,9 +456,25 @@ int launch_plan(const Plan& p, const void* packed, const uint16_t* scales, const
   return NQ_OK;
 }
 
-template <int BITS>
-void pack_host(const int8_t* codes, const uint16_t* scales, int64_t K, int64_t N, uint8_t* out,
-               uint16_t* sout) {
+// Identity row map: packed row n is row n of the inputs.
+struct PlainRows {
+  const int8_t* codes;
+  const uint16_t* scales;
+  const int8_t* code_row(int64_t n, int64_t K) const { return codes + n * K; }
+  const uint16_t* scale_row(int64_t n, int64_t G) const { return scales + n * G; }
+};
+// Gate/up interleaving of nq_pack_gate_up: packed row 16 r + m is gate row
+// 8 r + m and packed row 16 r + 8 + m is up row 8 r + m (m < 8).
+struct GateUpRows {
+  const int8_t *cg, *cu;
+  const uint16_t *sg, *su;
+  static int64_t src(int64_t n) { return (n >> 4) * 8 + (n & 7); }
+  const int8_t* code_row(int64_t n, int64_t K) const { return ((n & 8) ? cu : cg) + src(n) * K; }
+  const uint16_t* scale_row(int64_t n, int64_t G) const { return ((n & 8) ? su : sg) + src(n) * G; }
+};
+
+template <int BITS, class Rows>
+void pack_host(const Rows& rows, int64_t K, int64_t N, uint8_t* out, uint16_t* sout) {
   const int64_t G = K / kGroup, Nt = (N + kTileRows - 1) / kTileRows;
   constexpr uint32_t bias = 1u << (BITS - 1);
   for (int64_t rt = 0; rt < Nt; ++rt) {
@@ -470,7 +488,7 @@ void pack_host(const int8_t* codes, const uint16_t* scales, int64_t K, int64_t N
             int row, k;
             lane_code_coords(lane, p, h, &row, &k);
             const int64_t n = rt * kTileRows + row;
-            const int c = n < N ? codes[n * K + g * kGroup + k] : 0;
+            const int c = n < N ? rows.code_row(n, K)[g * kGroup + k] : 0;
             u[2 * p + h] = static_cast<uint32_t>(c + static_cast<int>(bias));
           }
         }
@@ -481,7 +499,7 @@ void pack_host(const int8_t* codes, const uint16_t* scales, int64_t K, int64_t N
       }
       for (int row = 0; row < kTileRows; ++row) {
         const int64_t n = rt * kTileRows + row;
-        sout[blk * 16 + 2 * (row & 7) + (row >> 3)] = n < N ? scales[n * G + g] : 0;
+        sout[blk * 16 + 2 * (row & 7) + (row >> 3)] = n < N ? rows.scale_row(n, G)[g] : 0;
       }
     }
   }
@@ -562,11 +580,37 @@ int nq_pack(const int8_t* codes, const uint16_t* scales, int64_t K, int64_t N, i
   for (int64_t i = 0; i < ns; ++i)
     if ((scales[i] & 0x7C00u) == 0x7C00u) return NQ_ERANGE;
   auto* out = static_cast<uint8_t*>(packed_out);
+  const PlainRows rows{codes, scales};
   switch (bits) {
-    case 4: pack_host<4>(codes, scales, K, N, out, scales_out); break;
-    case 5: pack_host<5>(codes, scales, K, N, out, scales_out); break;
-    case 8: pack_host<8>(codes, scales, K, N, out, scales_out); break;
-    default: pack_host<6>(codes, scales, K, N, out, scales_out); break;
+    case 4: pack_host<4>(rows, K, N, out, scales_out); break;
+    case 5: pack_host<5>(rows, K, N, out, scales_out); break;
+    case 8: pack_host<8>(rows, K, N, out, scales_out); break;
+    default: pack_host<6>(rows, K, N, out, scales_out); break;
+  }
+  return NQ_OK;
+}
+
+int nq_pack_gate_up(const int8_t* codes_gate, const uint16_t* scales_gate, const int8_t* codes_up,
+                    const uint16_t* scales_up, int64_t K, int64_t I, int bits, void* packed_out,
+                    uint16_t* scales_out) {
+  if (I <= 0 || I % 8 != 0) return NQ_EINVAL;
+  if (int rc = check_shape(K, 2 * I, bits)) return rc;
+  if (!codes_gate || !scales_gate || !codes_up || !scales_up || !packed_out || !scales_out)
+    return NQ_EINVAL;
+  const int lo = -(1 << (bits - 1)), hi = (1 << (bits - 1)) - 1;
+  for (const int8_t* c : {codes_gate, codes_up})
+    for (int64_t i = 0; i < K * I; ++i)
+      if (c[i] < lo || c[i] > hi) return NQ_ERANGE;
+  for (const uint16_t* sc : {scales_gate, scales_up})
+    for (int64_t i = 0; i < I * (K / kGroup); ++i)
+      if ((sc[i] & 0x7C00u) == 0x7C00u) return NQ_ERANGE;
+  auto* out = static_cast<uint8_t*>(packed_out);
+  const GateUpRows rows{codes_gate, codes_up, scales_gate, scales_up};
+  switch (bits) {
+    case 4: pack_host<4>(rows, K, 2 * I, out, scales_out); break;
+    case 5: pack_host<5>(rows, K, 2 * I, out, scales_out); break;
+    case 8: pack_host<8>(rows, K, 2 * I, out, scales_out); break;
+    default: pack_host<6>(rows, K, 2 * I, out, scales_out); break;
   }
   return NQ_OK;
 }

@@ -18,7 +18,7 @@ constexpr int kMergeWarps = 32;
 // are then merged pairwise in a tree.  Selection only, so the result does
 // not depend on the merge order.
 __global__ void __launch_bounds__(kMergeWarps * 32)
-    topk_merge_kernel(const unsigned long long* __restrict__ lists, int nlists, int k,
+    nq_topk_merge_kernel(const unsigned long long* __restrict__ lists, int nlists, int k,
                       int32_t* __restrict__ idx, float* __restrict__ val) {
   __shared__ unsigned long long part[kMergeWarps][32];
   griddep_wait();  // the lists are complete once the head GEMV has finished
@@ -56,7 +56,7 @@ cudaError_t launch_topk_merge(const unsigned long long* lists, int nlists, int T
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, topk_merge_kernel, lists, nlists, k, idx, val);
+  return cudaLaunchKernelEx(&cfg, nq_topk_merge_kernel, lists, nlists, k, idx, val);
 }
 
 }  // namespace nq

@@ -106,6 +106,39 @@ def test_head_ties_go_to_the_smallest_row():
     assert np.all(mx == 31.0 * K)
 
 
+@pytest.mark.parametrize("ksplit_rows", [(6, 256, 16 * 400), (5, 17408, 16 * 40)])
+def test_head_infinite_logits(ksplit_rows):
+    """Token 0 has x = +inf on one channel where every row's code is +1 or -1,
+    so its logits are +inf on a few rows spread over several CTAs (and
+    clusters) and -inf elsewhere: argmax is the first +inf row, the maximum
+    and logsumexp are +inf (merging two +inf states must not form inf - inf).
+    Token 1 is ordinary and must be unaffected."""
+    bits, K, N = ksplit_rows
+    rng = np.random.default_rng(77)
+    lo, hi = oracle.code_range(bits)
+    codes = rng.integers(lo, hi + 1, (N, K)).astype(np.int8)
+    plus = [37, N // 2 + 3, N - 1]
+    codes[:, 5] = -1
+    codes[plus, 5] = 1
+    sb = oracle.rtn_scales(rng.standard_normal((N, K)).astype(np.float32) * 0.02, oracle.QMAX[bits])
+    hp, hs = nqp.pack(codes, sb, bits)
+    packed, sp = torch.from_numpy(hp).to(DEV), torch.from_numpy(hs.view(np.int16)).to(DEV)
+    xb = ((rng.standard_normal((2, K)).astype(np.float32).view(np.uint32) >> 16)).astype(np.uint16)
+    xb[0, 5] = 0x7F80                                    # +inf
+    x = torch.from_numpy(xb.view(np.int16)).to(DEV).view(torch.bfloat16)
+    am, mx, lse = nqp.gemv_head(packed, sp, x, K, N, 2, bits)
+    assert nqp.last_device_error() == 0
+    am, mx, lse = am.cpu().numpy(), mx.cpu().numpy(), lse.cpu().numpy()
+    y_ref, e_ref = oracle.gemv(codes, sb, xb)
+    a_ref, m_ref, l_ref = oracle.head_reduce(y_ref)
+    assert a_ref[0] == plus[0] and m_ref[0] == np.inf and l_ref[0] == np.inf
+    assert am[0] == plus[0] and mx[0] == np.inf and lse[0] == np.inf
+    tol = oracle.REL_TOL * e_ref[1] + oracle.ABS_TOL
+    assert y_ref[1, am[1]] >= m_ref[1] - tol[am[1]] - tol[a_ref[1]]
+    assert abs(mx[1] - y_ref[1, am[1]]) <= tol[am[1]]
+    assert abs(lse[1] - l_ref[1]) <= tol.max() + LSE_ABS + LSE_REL * abs(l_ref[1])
+
+
 def test_head_workspace_errors():
     case = rtn_case((503,), 4, 64, 256, 1)
     packed, sp = device_weight(nqp, torch, case, DEV)

@@ -56,14 +56,19 @@ def _gate_up_case(tag, bits, I, H, T):
     return cg, sg, cu, su, xb, packed, sp
 
 
-def _check_act(act_bits, cg, sg, cu, su, xb):
-    g, e_g = oracle.gemv(cg, sg, xb)
-    u, e_u = oracle.gemv(cu, su, xb)
-    ref = oracle.bf16_to_f64(oracle.swiglu_bf16(g, u))
+def _check_act(act_bits, cg, sg, cu, su, xb, cd=None, sd=None):
+    """act against oracle.mlp (gate+up in (gate; up) row order); with down
+    weights, also returns the oracle's layer output and its error scale."""
+    if cd is None:                      # no down product: a zero matrix of K = I
+        cd = np.zeros((16, cg.shape[0]), np.int8)
+        sd = np.zeros((16, cg.shape[0] // 64), np.uint16)
+    act_ref, y_ref, e_ref, g, u, e_g, e_u = oracle.mlp(
+        np.concatenate([cg, cu]), np.concatenate([sg, su]), cd, sd, xb)
+    ref = oracle.bf16_to_f64(act_ref)
     got = oracle.bf16_to_f64(act_bits)
     tol = _act_tolerance(g, u, e_g, e_u)
     assert np.all(np.abs(got - ref) <= tol), np.max(np.abs(got - ref) / tol)
-    return ref, tol
+    return tol, y_ref, e_ref
 
 
 @pytest.mark.parametrize("bits,T", [(4, 1), (4, 2), (4, 8), (5, 3), (6, 16), (8, 4)])
@@ -99,9 +104,7 @@ def _check_layer(I, H, Hout, bits_gu, bits_down, T, tag):
     y = torch.full((T, Hout), float("nan"), dtype=torch.float32, device=DEV)
     nqp.mlp(gu, down, x, act, y, T)
     assert nqp.last_device_error() == 0
-    ref_act, tol_act = _check_act(act.cpu().numpy().view(np.uint16), cg, sg, cu, su, xb)
-    act_ref_bits = oracle.f64_to_bf16_bits(ref_act)
-    y_ref, e_ref = oracle.gemv(cd, sd, act_ref_bits)
+    tol_act, y_ref, e_ref = _check_act(act.cpu().numpy().view(np.uint16), cg, sg, cu, su, xb, cd, sd)
     w_abs = np.abs(oracle.dequant(cd, sd))
     bound = oracle.REL_TOL * e_ref + oracle.ABS_TOL + tol_act @ w_abs.T
     err = np.abs(y.cpu().numpy() - y_ref)

@@ -260,6 +260,25 @@ def test_q4_f16_route_x_edge_cases(T):
         _check_x(case, packed, sp, xb, name)
 
 
+@pytest.mark.parametrize("ksplit", [2, 4])
+@pytest.mark.parametrize("T", [1, 2])
+def test_q4_f16_route_with_k_split(T, ksplit):
+    """The fp16 route of 4-bit codes inside K-split clusters (the route the
+    4-bit down projections of the stack take at T <= 2): every x edge case
+    against the oracle, with the cluster's partial sums exchanged."""
+    case = rtn_case((316, T, ksplit), 4, 300, 4096, T)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    assert nqp.plan(4096, 300, T, 4, route=nqp.ROUTE_MMA, ksplit=ksplit)["ksplit"] == ksplit
+    for name, xb in _x_edge_cases(case["xb"]).items():
+        c = dict(case, xb=xb)
+        y = _y(c, packed, sp, route=nqp.ROUTE_MMA, ksplit=ksplit)
+        assert np.isfinite(y).all(), name
+        codes, sb = oracle_inputs(c)
+        y_ref, e_ref = oracle.gemv(codes, sb, xb)
+        v = oracle.max_violation(y, y_ref, e_ref)
+        assert v <= 1.0, (name, v)
+
+
 @pytest.mark.parametrize("T", [1, 2])
 def test_q4_f16_and_bf16_routes_agree(T, monkeypatch):
     """The same product through the fp16 route (default at T <= 2) and through
@@ -331,6 +350,8 @@ def test_max_t_long_k():
 FULL = {
     "gate_up_q4": ("rtn", 4, 34816, 5120, [1], 0.0),
     "down_q5": ("uniform", 5, 5120, 17408, [1, 8], 0.01),
+    # the 4-bit down projections of layers 36-63 of the 64-layer stack
+    "down_q4": ("rtn", 4, 5120, 17408, [1, 2, 4, 8, 16], 0.0),
     "head_q6": ("rtn", 6, 248320, 5120, [1, 2, 4, 8], 0.0),
     "down_q8": ("rtn", 8, 5120, 17408, [1, 8, 16], 0.0),
 }

@@ -161,3 +161,48 @@ def test_status_strings():
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert nqp.status_string(code) and nqp.status_string(code) != "unknown status"
     assert nqp.status_string(-99) == "unknown status"
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
+def test_pack_gate_up_interleaves_rows(bits):
+    """nq_pack_gate_up equals nq_pack of the row-interleaved matrix, and the
+    unpacked rows are gate row 8 r + m at 16 r + m, up row 8 r + m at
+    16 r + 8 + m."""
+    rng = synth.generator(0, 810, bits)
+    I, K = 40, 128
+    lo, hi = -(1 << (bits - 1)), (1 << (bits - 1)) - 1
+    cg = rng.integers(lo, hi + 1, (I, K)).astype(np.int8)
+    cu = rng.integers(lo, hi + 1, (I, K)).astype(np.int8)
+    sg = rng.integers(0, 0x7C00, (I, K // 64)).astype(np.uint16)
+    su = rng.integers(0, 0x7C00, (I, K // 64)).astype(np.uint16)
+    p, s = nqp.pack_gate_up(cg, sg, cu, su, bits)
+    p2, s2 = nqp.pack(nqp.interleave_gate_up(cg, cu), nqp.interleave_gate_up(sg, su), bits)
+    assert np.array_equal(p, p2) and np.array_equal(s, s2)
+    codes, scales = nqp.unpack(p, s, K, 2 * I, bits)
+    for n in range(2 * I):
+        r, m, up = n // 16, n % 8, (n % 16) >= 8
+        src_c, src_s = (cu, su) if up else (cg, sg)
+        assert np.array_equal(codes[n], src_c[8 * r + m]) and np.array_equal(scales[n], src_s[8 * r + m])
+
+
+def test_pack_gate_up_rejects_bad_arguments():
+    cg = np.zeros((12, 64), np.int8)
+    sg = np.zeros((12, 1), np.uint16)
+    with pytest.raises(nqp.NQError) as e:          # I not a multiple of 8
+        nqp.pack_gate_up(cg, sg, cg, sg, 4)
+    assert e.value.code == nqp.EINVAL
+    cg = np.zeros((8, 64), np.int8)
+    sg = np.zeros((8, 1), np.uint16)
+    bad = cg.copy()
+    bad[3, 7] = 8                                   # outside [-8, 7]
+    with pytest.raises(nqp.NQError) as e:
+        nqp.pack_gate_up(cg, sg, bad, sg, 4)
+    assert e.value.code == nqp.ERANGE
+
+
+def test_row_tile_count_limit():
+    """More than 2^31 - 1 row tiles is rejected (32-bit tile indices)."""
+    nqp.packed_bytes(64, 16 * (2 ** 31 - 1), 4)
+    with pytest.raises(nqp.NQError) as e:
+        nqp.packed_bytes(64, 16 * (2 ** 31 - 1) + 1, 4)
+    assert e.value.code == nqp.EINVAL

@@ -311,6 +311,18 @@ def test_head_logsumexp_large_logits_do_not_overflow():
     assert abs(lse[0] - (1000.0 + np.log(2.0 + np.exp(-1.0)))) <= 1e-12
 
 
+def test_head_infinite_logits():
+    """log(sum exp y) is +inf as soon as one logit is +inf (also with several),
+    and -inf logits contribute exp(-inf) = 0."""
+    inf = np.inf
+    y = np.array([[1.0, inf, 3.0, inf], [-inf, 2.0, -inf, 2.0], [inf, inf, inf, inf]])
+    am, m, lse = oracle.head_reduce(y)
+    assert am.tolist() == [1, 1, 0]
+    assert m.tolist() == [inf, 2.0, inf]
+    assert lse[0] == inf and lse[2] == inf
+    assert abs(lse[1] - (2.0 + np.log(2.0))) <= 1e-15
+
+
 def test_head_argmax_ties_take_the_first_index():
     y = np.array([[1.0, 5.0, 2.0, 5.0, 5.0], [7.0, 7.0, 7.0, 7.0, 7.0], [-1.0, -2.0, -1.0, -3.0, -1.5]])
     am, m, _ = oracle.head_reduce(y)
@@ -423,12 +435,52 @@ def test_search_picks_a_negative_scale_when_only_it_is_exact():
     assert s[0, 0] == 0x2000 and np.array_equal(c[0], vals)
 
 
+def _exact_candidates(a: float, qmax: int) -> list[int]:
+    """The 50 candidate scale patterns of the searched encoder's reading,
+    computed here in exact rational arithmetic (nearest FP16 by search, ties
+    to even): +h_i, -h_i for h_i = fp16(12 a / (12 (qmax + 1) - i))."""
+    out = []
+    for i in range(oracle.SEARCH_STEPS):
+        q = Fraction(12) * Fraction(float(a)) / (12 * (qmax + 1) - i)
+        h = 0 if q == 0 else _nearest_fp16_exact(q)
+        out += [h, h | 0x8000]
+    return out
+
+
+def test_search_candidates_worked_example():
+    """The hand-worked candidate lists of tests/golden (two group maxima)."""
+    with open(os.path.join(HERE, "golden", "search_candidates_worked_example.json")) as f:
+        g = json.load(f)
+    for case in g["cases"]:
+        a, qmax = float(case["absmax"]), case["qmax"]
+        assert qmax == oracle.QMAX[case["bits"]]
+        want = []
+        for i, den, m, plus, minus in case["candidates"]:
+            assert den == 12 * (qmax + 1) - i
+            want += [int(plus, 16), int(minus, 16)]
+        got = oracle.search_candidates(np.array([a]), qmax)[0]
+        assert [int(v) for v in got] == want
+        assert _exact_candidates(a, qmax) == want
+
+
+def test_search_candidates_exact_over_binades():
+    """oracle.search_candidates against exact rational rounding for group
+    maxima spread over the FP16 range (subnormal scales included)."""
+    rng = np.random.default_rng(905)
+    a = (rng.uniform(1.0, 2.0, 60) * 2.0 ** rng.integers(-22, 15, 60)).astype(np.float32)
+    for bits in (4, 5, 6, 8):
+        qmax = oracle.QMAX[bits]
+        cand = oracle.search_candidates(a.astype(np.float64), qmax)
+        for ai, row in zip(a, cand):
+            assert [int(v) for v in row] == _exact_candidates(float(ai), qmax), (bits, ai)
+
+
 def test_search_ties_go_to_the_first_candidate():
     rng = synth.generator(0, 901)
     w = synth.gauss_weights(rng, 2, 64)
     c, s = oracle.search_encode(w, 5, imatrix=np.zeros(64, np.float32))   # every error 0
-    cand = oracle.search_candidates(np.abs(w.astype(np.float64)).max(axis=1), 15)
-    assert np.array_equal(s[:, 0], cand[:, 0])
+    for r in range(2):
+        assert s[r, 0] == _exact_candidates(float(np.abs(w[r]).max()), 15)[0]
     z = np.zeros((1, 128), np.float32)
     c, s = oracle.search_encode(z, 6)
     assert np.all(s == 0) and np.all(c == 0)
@@ -447,8 +499,7 @@ def test_search_single_important_channel_matches_exact_brute_force():
             q = np.zeros(64, np.float32)
             q[j] = 1.0
             c, s = oracle.search_encode(w, bits, q)
-            cand = oracle.search_candidates(np.array([np.abs(w.astype(np.float64)).max()]),
-                                            oracle.QMAX[bits])[0]
+            cand = _exact_candidates(float(np.abs(w).max()), oracle.QMAX[bits])
             wj = Fraction(float(w[0, j]))
             errs = []
             for b in cand:
@@ -512,3 +563,77 @@ def test_silu_identities():
     act = oracle.swiglu_bf16(g, np.ones_like(g))
     assert np.array_equal(act, oracle.f64_to_bf16_bits(s))
     assert np.all(oracle.bf16_to_f64(oracle.swiglu_bf16(np.zeros(5), np.arange(5.0))) == 0.0)
+
+
+# ---------------------------------------------------------------- the layer MLP
+def _one_hot_mlp_case():
+    """A layer with H = 64 (one group), I = 64, H_out = 16 whose every value is
+    known in closed form: x is one-hot at k = 5 with value 1, so gate[i] and
+    up[i] are scale * code of column 5; gates are +-64 or 0, ups small
+    dyadic values, and the down weights 0.25 times small codes."""
+    H, I, Ho = 64, 64, 16
+    gate_codes = [4, 4, -4, 0, 4, -4, 4, 4] + [0] * (I - 8)   # gate = 16 c: 64, 64, -64, 0, ...
+    up_codes = [3, -5, 7, 6, 1, 2, -8, 0] + [1] * (I - 8)     # up = 0.5 c
+    cg = np.zeros((I, H), np.int8)
+    cu = np.zeros((I, H), np.int8)
+    cg[:, 5] = gate_codes
+    cu[:, 5] = up_codes
+    sg = np.full((I, 1), 0x4C00, np.uint16)             # 16.0
+    su = np.full((I, 1), 0x3800, np.uint16)             # 0.5
+    x = np.zeros((1, H), np.uint16)
+    x[0, 5] = 0x3F80                                      # bf16 1.0
+    rng = np.random.default_rng(31)
+    cd = rng.integers(-8, 8, (Ho, I)).astype(np.int8)
+    sd = np.full((Ho, 1), 0x3400, np.uint16)            # 0.25
+    return cg, sg, cu, su, cd, sd, x, gate_codes, up_codes
+
+
+def test_mlp_closed_form():
+    """oracle.mlp on a one-hot layer: silu(64) = 64 and silu(0) = 0 exactly in
+    fp64, silu(-64) = -64 / (1 + e^64) (below 1e-25), so act = bf16(64 u) is
+    exact, act for a zero gate is 0, and y = sum_i w_down[:, i] act[i] is
+    checked in exact rational arithmetic."""
+    cg, sg, cu, su, cd, sd, x, gcodes, ucodes = _one_hot_mlp_case()
+    I = len(gcodes)
+    act, y, e, gate, up, e_g, e_u = oracle.mlp(np.concatenate([cg, cu]), np.concatenate([sg, su]),
+                                               cd, sd, x)            # (gate; up) row order
+    assert act.shape == (1, I) and y.shape == (1, cd.shape[0])
+    assert list(gate[0]) == [16.0 * c for c in gcodes]
+    assert list(up[0]) == [0.5 * c for c in ucodes]
+    a = oracle.bf16_to_f64(act[0])
+    for i in range(I):
+        u = 0.5 * ucodes[i]
+        if gcodes[i] > 0:
+            assert a[i] == 64.0 * u                      # exact in bf16 (small dyadic)
+        elif gcodes[i] == 0:
+            assert a[i] == 0.0
+        else:
+            assert abs(a[i]) < 1e-25 * max(1.0, abs(u))
+            assert a[i] == 0.0 or np.sign(a[i]) == -np.sign(u)
+    # y in exact rationals from those activations: every term is a dyadic
+    # rational with few bits, so the fp64 sums are exact up to the tiny
+    # negative-gate terms
+    for n in range(cd.shape[0]):
+        ref = sum(Fraction(int(cd[n, i]), 4) * Fraction(float(a[i])) for i in range(I))
+        assert abs(Fraction(float(y[0, n])) - ref) <= Fraction(1, 10 ** 20)
+        big = sum(Fraction(int(cd[n, i]), 4) * Fraction(float(a[i])) for i in range(I) if gcodes[i] > 0)
+        assert abs(Fraction(float(y[0, n])) - big) <= Fraction(1, 10 ** 20)
+
+
+def test_mlp_planted_mistakes_are_caught():
+    """Swapping the gate and up halves, or skipping the bf16 rounding of act,
+    changes the closed-form result of test_mlp_closed_form."""
+    cg, sg, cu, su, cd, sd, x, gcodes, ucodes = _one_hot_mlp_case()
+    act, y, *_ = oracle.mlp(np.concatenate([cg, cu]), np.concatenate([sg, su]), cd, sd, x)
+    act_sw, y_sw, *_ = oracle.mlp(np.concatenate([cu, cg]), np.concatenate([su, sg]), cd, sd, x)
+    assert not np.array_equal(act, act_sw) and not np.array_equal(y, y_sw)
+    # a layer that rounds act only after the down product would differ where
+    # silu(g) u is not a bf16 value: g = 1 gives silu(1) = 0.7310585786...
+    cg1 = cg.copy()
+    cg1[:, 5] = 0
+    cg1[0, 5] = 1
+    sg1 = np.full_like(sg, 0x3C00)                       # 1.0: gate[0] = 1
+    act1, y1, *_ = oracle.mlp(np.concatenate([cg1, cu]), np.concatenate([sg1, su]), cd, sd, x)
+    exact_act0 = 1.0 / (1.0 + np.exp(-1.0)) * (0.5 * ucodes[0])
+    assert oracle.bf16_to_f64(act1[0, 0]) != exact_act0
+    assert abs(oracle.bf16_to_f64(act1[0, 0]) - exact_act0) <= abs(exact_act0) * 2.0 ** -8   # half a bf16 step
