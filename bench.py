@@ -10,9 +10,15 @@ x is seeded N(0, 1) in bf16.  A step is one pass over the whole stack at each
 T (4 x 129 GEMVs, 41.9 GB of packed weights), inputs resident in HBM.
 
 The GEMVs of a pass are independent (no activation between them), so each
-pass is grouped by tensor kind: the 64 gate+up GEMVs, the 64 down GEMVs, the
-head; each group is one CUDA graph, and CUDA events between the groups give
-the average launch duration of each kernel inside the timed region.
+pass is grouped by tensor kind: the 64 gate+up GEMVs, the 36 5-bit and the 28
+4-bit down GEMVs, the head; each group is one CUDA graph, and CUDA events
+between the groups give the duration of each kind inside the timed region
+(mean, median and minimum over the timed steps).
+
+After timing, every graph is replayed once more per T and sampled rows of the
+outputs it wrote (the last GEMV of the group) are compared with the CPU oracle
+on the same weights and x; a mismatch fails the run.  The oracle is also timed
+on the host cores (one core, and every core of the process's affinity mask).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -21,7 +27,8 @@ on a bounded sample of the same workload instead.
 """
 from __future__ import annotations
 
-# The CPU oracle is timed single-threaded; fix BLAS threads before numpy loads.
+# The CPU oracle runs one BLAS thread per process; fix it before numpy loads
+# (spawned worker processes inherit the setting).
 import os
 
 for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
@@ -30,6 +37,7 @@ for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
 import argparse
 import hashlib
 import json
+import multiprocessing
 import statistics
 import subprocess
 import sys
@@ -40,8 +48,9 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-HIDDEN, INTER, VOCAB, LAYERS = 5120, 17408, 248320, 64
+HIDDEN, INTER, VOCAB, LAYERS, Q5_LAYERS = 5120, 17408, 248320, 64, 36
 TS = (1, 4, 8, 16)
+KINDS = ("gate_up", "down_q5", "down_q4", "head")
 METRIC = "quantized GEMV weight-stream GB/s and % of GB300 HBM peak, T=1/8/16"
 UNIT = "GB/s"
 
@@ -52,7 +61,8 @@ def stack_tensors():
     for l in range(LAYERS):
         out.append(("gate_up", l, 4, HIDDEN, 2 * INTER))
     for l in range(LAYERS):
-        out.append(("down", l, 5 if l < 36 else 4, INTER, HIDDEN))
+        out.append(("down_q5" if l < Q5_LAYERS else "down_q4", l, 5 if l < Q5_LAYERS else 4,
+                    INTER, HIDDEN))
     out.append(("head", 0, 6, HIDDEN, VOCAB))
     return out
 
@@ -64,7 +74,8 @@ def packed_bytes(bits, K, N):
 
 PASS_BYTES = sum(packed_bytes(b, K, N) for (_, _, b, K, N) in stack_tensors())
 KIND_BYTES = {k: sum(packed_bytes(b, K, N) for (kk, _, b, K, N) in stack_tensors() if kk == k)
-              for k in ("gate_up", "down", "head")}
+              for k in KINDS}
+KIND_COUNT = {k: sum(1 for e in stack_tensors() if e[0] == k) for k in KINDS}
 CONFIG = {
     "workload": "64-layer Qwen3.8-27B-shaped MLP+head weight stream: per layer gate+up Q4 "
                 "5120x34816 and down 17408x5120 (Q5 layers 0-35, Q4 36-63), then the Q6 head "
@@ -74,6 +85,9 @@ CONFIG = {
     "l2": "inputs larger than L2 (10.49 GB of distinct packed weights per pass, L2 129 MB)",
     "launch": "one CUDA graph per tensor kind and T, programmatic dependent launch",
 }
+# Rows of the last tensor of each kind whose outputs are checked against the
+# oracle (and on which the oracle is timed).
+CHECK_ROWS = {"gate_up": 96, "down_q5": 24, "down_q4": 24, "head": 64}
 
 
 def source_hash() -> str:
@@ -182,15 +196,18 @@ def whole_job_gbs(world: int, steps: int, bytes_per_step: int, ms: float) -> flo
 
 
 # ------------------------------------------------------------------ CPU oracle leg
+SAMPLE_ROWS = {"gate_up": (4, HIDDEN, 96), "down": (5, INTER, 16), "head": (6, HIDDEN, 64)}
+
+
 def oracle_sample(seconds: float, seed: int = 77):
-    """Time the CPU oracle (fp64) on sampled rows of the same workload: rows of
-    the gate+up, down and head tensors at T = 1, 4, 8, 16, in proportion to their
-    bytes.  Returns (GB/s of packed-weight bytes, bytes, seconds, description)."""
+    """Time the CPU oracle (fp64, this process, one BLAS thread) on sampled rows
+    of the same workload: rows of the gate+up, down and head tensors at T = 1,
+    4, 8, 16, in proportion to their bytes.  Returns (GB/s of packed-weight
+    bytes, bytes, seconds, description)."""
     import oracle
     import synth
-    rows = {"gate_up": (4, HIDDEN, 96), "down": (5, INTER, 16), "head": (6, HIDDEN, 64)}
     prepared = []
-    for i, (kind, (bits, K, n)) in enumerate(rows.items()):
+    for i, (kind, (bits, K, n)) in enumerate(SAMPLE_ROWS.items()):
         rng = synth.generator(seed, 700 + i)
         w = synth.gauss_weights(rng, n, K)
         codes, sb = oracle.rtn_encode(w, bits)
@@ -206,32 +223,74 @@ def oracle_sample(seconds: float, seed: int = 77):
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    desc = (f"oracle.gemv (fp64, single thread) on {reps} rounds of sampled rows "
+    desc = (f"oracle.gemv (fp64 numpy, one BLAS thread per process) on rounds of sampled rows "
             f"(gate+up 96 rows, down 16 rows, head 64 rows) at T=1,4,8,16")
     return done_bytes / el / 1e9, done_bytes, el, desc
+
+
+def _oracle_worker(args):
+    seconds, seed = args
+    _, nbytes, el, _ = oracle_sample(seconds, seed)
+    return nbytes, el
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_pool():
+    """One spawned worker process per core of the affinity mask (each with one
+    BLAS thread); spawned, not forked, so a process that uses the GPU can
+    start it."""
+    n = host_cores()
+    return multiprocessing.get_context("spawn").Pool(n), n
+
+
+def oracle_all_cores(pool, n: int, seconds: float, seed: int = 77):
+    """The sample on every worker at once, each timed over `seconds`.
+    Returns (bytes summed over the workers, the slowest worker's seconds)."""
+    res = pool.map(_oracle_worker, [(seconds, seed + i) for i in range(n)])
+    return sum(b for b, _ in res), max(e for _, e in res)
+
+
+def cpu_baseline(seconds: float):
+    single, _, _, desc = oracle_sample(seconds)
+    pool, n = oracle_pool()
+    with pool:
+        oracle_all_cores(pool, n, 0.2)                      # workers started and warm
+        nbytes, el = oracle_all_cores(pool, n, seconds)
+    return {"value": round(nbytes / el / 1e9, 4), "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": desc + f"; {seconds:.1f} s on every core (one process each)",
+            "single_core": {"value": round(single, 4), "cores": 1}}
 
 
 def run_reference(args, rank):
     if rank != 0:
         return
     per_step = max(0.5, args.ref_step_seconds)
-    for _ in range(args.warmup):
-        oracle_sample(per_step / 4)
-    t0 = time.perf_counter()
-    total_bytes = 0
-    desc = ""
-    for _ in range(args.steps):
-        _, b, _, desc = oracle_sample(per_step)
-        total_bytes += b
-    el = time.perf_counter() - t0
+    pool, n = oracle_pool()
+    with pool:
+        for _ in range(args.warmup):
+            oracle_all_cores(pool, n, per_step / 4)
+        t0 = time.perf_counter()
+        total_bytes = 0
+        for _ in range(args.steps):
+            nbytes, _ = oracle_all_cores(pool, n, per_step)
+            total_bytes += nbytes
+        el = time.perf_counter() - t0
     value = total_bytes / el / 1e9
+    _, _, _, desc = oracle_sample(0.0)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": CONFIG,
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": desc + f"; {per_step:.1f} s per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": n, "kind": "oracle",
+                         "sample": desc + f"; {per_step:.1f} s per step on every core "
+                                          "(one process each)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -239,16 +298,24 @@ def run_reference(args, rank):
 
 # ------------------------------------------------------------------ GPU leg
 def build_stack(torch, nqp, dev, seed):
-    """Packed weights of every tensor, x arena (16 tokens per GEMV), y buffers."""
+    """Packed weights of every tensor, x arena (16 tokens per GEMV), y buffers;
+    the fp32 rows of each kind's last tensor that the oracle check uses."""
     entries = []
+    rng = np.random.default_rng(seed + 12345)
+    last = {k: max(i for i, e in enumerate(stack_tensors()) if e[0] == k) for k in KINDS}
     for idx, (kind, layer, bits, K, N) in enumerate(stack_tensors()):
         g = torch.Generator(device=dev)
         g.manual_seed(seed * 1000003 + idx)
         w = torch.randn((N, K), generator=g, device=dev, dtype=torch.float32)
         w.mul_(0.02)
         qw = nqp.QuantizedWeight.from_fp32(w, bits)
+        e = {"kind": kind, "layer": layer, "bits": bits, "K": K, "N": N, "qw": qw}
+        if idx == last[kind]:
+            rows = np.unique(np.concatenate([[0, 15, N - 1], rng.choice(N, CHECK_ROWS[kind], replace=False)]))
+            e["check_rows"] = rows
+            e["check_w"] = w[torch.from_numpy(rows).to(dev)].cpu().numpy()
         del w
-        entries.append({"kind": kind, "layer": layer, "bits": bits, "K": K, "N": N, "qw": qw})
+        entries.append(e)
     torch.cuda.synchronize()
     rc = nqp.last_device_error()
     if rc != 0:
@@ -264,8 +331,51 @@ def build_stack(torch, nqp, dev, seed):
     for e, o in zip(entries, offs):
         e["x"] = x_arena[o:o + 16 * e["K"]].view(16, e["K"])
     ys = {k: torch.empty((16, n), dtype=torch.float32, device=dev)
-          for k, n in (("gate_up", 2 * INTER), ("down", HIDDEN), ("head", VOCAB))}
+          for k, n in (("gate_up", 2 * INTER), ("down_q5", HIDDEN), ("down_q4", HIDDEN),
+                       ("head", VOCAB))}
     return entries, x_arena, ys
+
+
+def capture(torch, nqp, entries, ys, T, kind, stream):
+    sel = [e for e in entries if e["kind"] == kind]
+
+    def run():
+        for e in sel:
+            nqp.gemv(e["qw"].packed, e["qw"].scales, e["x"][:T], ys[kind][:T], e["K"], e["N"], T,
+                     e["bits"], stream=stream)
+    with torch.cuda.stream(stream):
+        run()                                     # plans cached, attributes set
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run()
+    return g, len(sel)
+
+
+def check_outputs(torch, nqp, entries, ys, graphs, stream):
+    """Replay every graph once per T and compare sampled rows of the output it
+    wrote (its last GEMV) with the oracle on the same fp32 weights and x.
+    Returns {kind_T: largest tolerance ratio} (<= 1 passes)."""
+    import oracle
+    out = {}
+    for e in entries:
+        if "check_rows" not in e:
+            continue
+        codes, sb = oracle.rtn_encode(e["check_w"], e["bits"])
+        xb = e["x"].view(torch.int16).cpu().numpy().view(np.uint16)
+        for T in TS:
+            ys[e["kind"]].fill_(float("nan"))
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                graphs[(T, e["kind"])].replay()
+            torch.cuda.synchronize()
+            y = ys[e["kind"]][:T].cpu().numpy()[:, e["check_rows"]]
+            y_ref, e_ref = oracle.gemv(codes, sb, xb[:T])
+            out[f"{e['kind']}_T{T}"] = round(oracle.max_violation(y, y_ref, e_ref), 6)
+    rc = nqp.last_device_error(stream)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} in the output check")
+    return out
 
 
 def _graph_us(torch, stream, run, reps):
@@ -299,7 +409,7 @@ def fused_head_times(torch, nqp, entries, stream, reps):
     dev = e["x"].device
     ws = torch.empty(nqp.head_topk_workspace_bytes(), dtype=torch.uint8, device=dev)
     out = {}
-    for T in TS:
+    for T in (1, 2, 4, 8, 16):
         res = [torch.empty(T, dtype=dt, device=dev) for dt in (torch.int32, torch.float32, torch.float32)]
         tk_idx = torch.empty(T * 32, dtype=torch.int32, device=dev)    # [T, k] row-major
         tk_val = torch.empty(T * 32, dtype=torch.float32, device=dev)
@@ -326,53 +436,58 @@ def fused_head_times(torch, nqp, entries, stream, reps):
     return out
 
 
+def head_t2_time(torch, nqp, entries, ys, stream, reps):
+    """The plain head GEMV at T = 2 (a verify batch the stack does not run),
+    one launch per graph replay: microseconds and GB/s."""
+    e = next(x for x in entries if x["kind"] == "head")
+
+    def run():
+        nqp.gemv(e["qw"].packed, e["qw"].scales, e["x"][:2], ys["head"][:2], e["K"], e["N"], 2,
+                 e["bits"], stream=stream)
+    us = _graph_us(torch, stream, run, reps)
+    return {"us_per_launch": round(us, 2), "gbs": round(KIND_BYTES["head"] / (us * 1e-6) / 1e9, 1)}
+
+
 def mlp_times(torch, nqp, entries, stream, reps):
-    """One layer's MLP through nq_mlp (gate+up with SwiGLU in the epilogue,
-    then the down projection, programmatic dependent launch between them) at
-    every T, one CUDA graph per T, against the same two GEMVs launched plainly
-    (fp32 gate and up stored, no activation).  Weight bytes per layer / time.
-    (The stack's gate+up rows are not in the interleaved order a real layer
-    would use; the work, and so the time, is the same.)"""
-    gu = next(e for e in entries if e["kind"] == "gate_up")
-    dn = next(e for e in entries if e["kind"] == "down" and e["layer"] == 0)
-    dev = gu["x"].device
-    nbytes = (packed_bytes(gu["bits"], gu["K"], gu["N"]) + packed_bytes(dn["bits"], dn["K"], dn["N"]))
+    """The 64 decoder-layer MLPs through nq_mlp (gate+up with SwiGLU in the
+    epilogue, its bf16 activations feeding the down projection) chained in
+    one CUDA graph per T: the library's choice (two launches per layer) and,
+    where it applies (T <= 8), the one-launch layer kernel; against the same
+    128 GEMVs launched plainly (fp32 gate and up stored, independent x).  Per-layer microseconds and weight-stream
+    GB/s.  (The stack's gate+up rows are not in the interleaved order a real
+    layer uses; the work, and so the time, is the same.)"""
+    gus = [e for e in entries if e["kind"] == "gate_up"]
+    dns = [e for e in entries if e["kind"] in ("down_q5", "down_q4")]
+    dev = gus[0]["x"].device
+    nbytes = KIND_BYTES["gate_up"] + KIND_BYTES["down_q5"] + KIND_BYTES["down_q4"]
     act = torch.empty((16, INTER), dtype=torch.int16, device=dev)
-    y1 = torch.empty((16, gu["N"]), dtype=torch.float32, device=dev)
-    y = torch.empty((16, dn["N"]), dtype=torch.float32, device=dev)
+    y1 = torch.empty((16, 2 * INTER), dtype=torch.float32, device=dev)
+    y = torch.empty((16, HIDDEN), dtype=torch.float32, device=dev)
     out = {}
     for T in TS:
-        def fused():
-            nqp.mlp(gu["qw"], dn["qw"], gu["x"][:T], act[:T], y[:T], T, stream=stream)
+        def layers(launches):
+            def run():
+                for gu, dn in zip(gus, dns):
+                    nqp.mlp(gu["qw"], dn["qw"], gu["x"][:T], act[:T], y[:T], T, launches=launches,
+                            stream=stream)
+            return run
 
         def plain():
-            nqp.gemv(gu["qw"].packed, gu["qw"].scales, gu["x"][:T], y1[:T], gu["K"], gu["N"], T,
-                     gu["bits"], stream=stream)
-            nqp.gemv(dn["qw"].packed, dn["qw"].scales, act[:T].view(torch.bfloat16), y[:T], dn["K"],
-                     dn["N"], T, dn["bits"], stream=stream)
-        res = {}
-        for name, fn in (("fused_us", fused), ("two_gemv_us", plain)):
-            with torch.cuda.stream(stream):
-                fn()
-            stream.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                fn()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                g.replay()
-                e0.record(stream)
-                for _ in range(reps):
-                    g.replay()
-                e1.record(stream)
-            stream.synchronize()
-            res[name] = round(e0.elapsed_time(e1) * 1e3 / reps, 2)
-        res["fused_gbs"] = round(nbytes / (res["fused_us"] * 1e-6) / 1e9, 1)
+            for gu, dn in zip(gus, dns):
+                nqp.gemv(gu["qw"].packed, gu["qw"].scales, gu["x"][:T], y1[:T], gu["K"], gu["N"], T,
+                         gu["bits"], stream=stream)
+                nqp.gemv(dn["qw"].packed, dn["qw"].scales, dn["x"][:T], y[:T], dn["K"], dn["N"], T,
+                         dn["bits"], stream=stream)
+        res = {"mlp_us_per_layer": round(_graph_us(torch, stream, layers(0), reps) / LAYERS, 2)}
+        if all(nqp.mlp_one_launch_ok(HIDDEN, INTER, HIDDEN, T, 4, b) for b in (5, 4)):
+            res["one_launch_us_per_layer"] = round(_graph_us(torch, stream, layers(1), reps) / LAYERS, 2)
+        res["two_gemv_us_per_layer"] = round(_graph_us(torch, stream, plain, reps) / LAYERS, 2)
+        res["mlp_gbs"] = round(nbytes / LAYERS / (res["mlp_us_per_layer"] * 1e-6) / 1e9, 1)
+        res["mlp_frac"] = round(res["mlp_gbs"] / measured_peaks()[0], 4)
         out[f"T{T}"] = res
     rc = nqp.last_device_error(stream)
     if rc != 0:
-        raise RuntimeError(f"device status {rc} in the MLP layer")
+        raise RuntimeError(f"device status {rc} in the MLP layers")
     return out
 
 
@@ -418,20 +533,8 @@ def encoder_times(torch, nqp, dev, reps=3):
     return out
 
 
-def capture(torch, nqp, entries, ys, T, kind, stream):
-    sel = [e for e in entries if e["kind"] == kind]
-
-    def run():
-        for e in sel:
-            nqp.gemv(e["qw"].packed, e["qw"].scales, e["x"][:T], ys[kind][:T], e["K"], e["N"], T,
-                     e["bits"], stream=stream)
-    with torch.cuda.stream(stream):
-        run()                                     # plans cached, attributes set
-    stream.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        run()
-    return g, len(sel)
+def _stats(vals):
+    return {"mean": statistics.fmean(vals), "median": statistics.median(vals), "min": min(vals)}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -452,11 +555,10 @@ def run_ours(args, rank, world, local_rank):
 
     entries, x_arena, ys = build_stack(torch, nqp, dev, seed=args.seed + rank)
     stream = torch.cuda.Stream(device=dev)
-    kinds = ("gate_up", "down", "head")
     graphs = {}
     launches_per_pass = 0
     for T in TS:
-        for k in kinds:
+        for k in KINDS:
             graphs[(T, k)], n = capture(torch, nqp, entries, ys, T, k, stream)
             if T == TS[0]:
                 launches_per_pass += n
@@ -466,7 +568,7 @@ def run_ours(args, rank, world, local_rank):
 
     def one_step(evs=None):
         for T in TS:
-            for k in kinds:
+            for k in KINDS:
                 graphs[(T, k)].replay()
                 if evs is not None:
                     evs[(T, k)].append(torch.cuda.Event(enable_timing=True))
@@ -498,21 +600,27 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device status {rc} in timed region")
     total_ms = max_over_ranks(start.elapsed_time(end), dev)
 
-    # per-(T, kind) durations from consecutive events
-    seg = {key: 0.0 for key in graphs}
+    # per-(T, kind) durations of every step, from consecutive events
+    seg = {key: [] for key in graphs}
     prev = start
     for s in range(args.steps):
         for T in TS:
-            for k in kinds:
+            for k in KINDS:
                 e = evs[(T, k)][s]
-                seg[(T, k)] += prev.elapsed_time(e)
+                seg[(T, k)].append(prev.elapsed_time(e))
                 prev = e
 
-    # ---------------- fused verify head (argmax, maximum, logsumexp per token)
-    head_fused = fused_head_times(torch, nqp, entries, stream, reps=max(10, min(args.steps, 50)))
+    # ---------------- outputs of the timed graphs against the oracle
+    checks = check_outputs(torch, nqp, entries, ys, graphs, stream)
+    checked = all(v <= 1.0 for v in checks.values())
 
-    # ---------------- one decoder-layer MLP: SwiGLU product then down (nq_mlp)
-    mlp_layer = mlp_times(torch, nqp, entries, stream, reps=max(10, min(args.steps, 50)))
+    # ---------------- fused verify head (argmax, maximum, logsumexp per token)
+    reps = max(10, min(args.steps, 50))
+    head_fused = fused_head_times(torch, nqp, entries, stream, reps=reps)
+    head_t2 = head_t2_time(torch, nqp, entries, ys, stream, reps=reps)
+
+    # ---------------- the 64 decoder-layer MLPs: SwiGLU product then down (nq_mlp)
+    mlp_layers = mlp_times(torch, nqp, entries, stream, reps=max(3, min(args.steps, 10)))
 
     # ---------------- offline encoders on one gate+up-sized matrix
     encoders = encoder_times(torch, nqp, dev) if rank == 0 else None
@@ -533,7 +641,7 @@ def run_ours(args, rank, world, local_rank):
         for _ in range(e2e_steps):
             x_arena.copy_(x_host, non_blocking=True)
             for T in TS:
-                for k in kinds:
+                for k in KINDS:
                     graphs[(T, k)].replay()
                 y_host[T].copy_(ys["head"][:T], non_blocking=True)
         e1.record(stream)
@@ -542,35 +650,52 @@ def run_ours(args, rank, world, local_rank):
 
     if rank != 0:
         return
+    if not checked:
+        print(json.dumps({"error": "GPU outputs outside the oracle's tolerance", "checks": checks}),
+              file=sys.stderr, flush=True)
+        sys.exit(3)
     peak, peak_kind = measured_peaks()
     steps = args.steps
     value = whole_job_gbs(world, steps, len(TS) * PASS_BYTES, total_ms)
     e2e_value = whole_job_gbs(world, e2e_steps, len(TS) * PASS_BYTES, e2e_ms)
     per_t = {}
     for T in TS:
-        ms = sum(seg[(T, k)] for k in kinds) / steps
-        gbs = PASS_BYTES / (ms * 1e-3) / 1e9
-        per_t[str(T)] = {"us_per_pass": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+        ms = [sum(seg[(T, k)][s] for k in KINDS) for s in range(steps)]
+        st = _stats(ms)
+        gbs = PASS_BYTES / (st["mean"] * 1e-3) / 1e9
+        per_t[str(T)] = {"us_per_pass": round(st["mean"] * 1e3, 2),
+                         "us_per_pass_median": round(st["median"] * 1e3, 2),
+                         "us_per_pass_min": round(st["min"] * 1e3, 2), "gbs": round(gbs, 1),
                          "frac_of_measured_hbm": round(gbs / peak, 4),
                          "frac_of_8tbs": round(gbs / 8000.0, 4)}
     kernels = {}
     for T in TS:
-        for k in kinds:
-            n = sum(1 for e in entries if e["kind"] == k)
-            us = seg[(T, k)] / steps / n * 1e3
-            gbs = KIND_BYTES[k] / n / (us * 1e-6) / 1e9
-            kernels[f"{k}_T{T}"] = {"us_per_launch": round(us, 2), "gbs": round(gbs, 1),
-                                    "frac": round(gbs / peak, 4)}
+        for k in KINDS:
+            n = KIND_COUNT[k]
+            st = _stats([v * 1e3 / n for v in seg[(T, k)]])       # us per launch, per step
+            gbs = KIND_BYTES[k] / n / (st["mean"] * 1e-6) / 1e9
+            kernels[f"{k}_T{T}"] = {
+                "us_per_launch": round(st["mean"], 2), "us_median": round(st["median"], 2),
+                "us_min": round(st["min"], 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                "frac_of_min": round(KIND_BYTES[k] / n / (st["min"] * 1e-6) / 1e9 / peak, 4)}
     dom = kernels["gate_up_T1"]
     roofline = {"bound": "hbm", "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
                 "frac": round(dom["gbs"] / peak, 4), "traffic": stored_traffic(),
-                "kernel": "gemv_kernel<4,1,3> (4-bit, MMA route, x in registers) "
+                "kernel": "nq_gemv_kernel<4,1,3> (4-bit, MMA route, x in registers) "
                           "gate+up Q4 K=5120 N=34816 at T=1",
                 "bytes_per_launch": packed_bytes(4, HIDDEN, 2 * INTER),
                 "peak_source": peak_kind,
-                # the same product at every T of the step (T=16: gemv_kernel<4,1,4>)
+                # the same product at every T of the step (T=16: nq_gemv_kernel<4,1,4>)
                 "frac_by_T": {str(T): kernels[f"gate_up_T{T}"]["frac"] for T in TS}}
-    cpu_v, _, cpu_s, cpu_desc = oracle_sample(args.cpu_seconds)
+    # The single-shape configurations inside the stack (each kind's graph at T).
+    configs = {
+        "gate_up_q4_T1": kernels["gate_up_T1"]["frac"],
+        "down_q5_T1": kernels["down_q5_T1"]["frac"], "down_q5_T8": kernels["down_q5_T8"]["frac"],
+        "down_q5_T16": kernels["down_q5_T16"]["frac"],
+        "head_q6_T1": kernels["head_T1"]["frac"], "head_q6_T2": round(head_t2["gbs"] / peak, 4),
+        "head_q6_T4": kernels["head_T4"]["frac"], "head_q6_T8": kernels["head_T8"]["frac"],
+        "head_q6_T16": kernels["head_T16"]["frac"],
+    }
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / steps, 4), "higher_is_better": True,
@@ -580,16 +705,19 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": steps * len(TS) * launches_per_pass,
         "roofline": roofline,
-        "cpu_baseline": {"value": round(cpu_v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": cpu_desc + f" for {cpu_s:.1f} s"},
+        "cpu_baseline": cpu_baseline(args.cpu_seconds),
         "clocks": clocks,
+        "checked": checked,
+        "checks": checks,
         "per_T": per_t,
         "kernels": kernels,
+        "configs_frac_of_measured": configs,
         "head_fused": head_fused,
-        "mlp_layer": mlp_layer,
+        "head_T2": head_t2,
+        "mlp_layers": mlp_layers,
         "encoders": encoders,
         "plans": {f"{k}_T{T}": nqp.plan(e["K"], e["N"], T, e["bits"])
-                  for T in TS for k in kinds
+                  for T in TS for k in KINDS
                   for e in [next(x for x in entries if x["kind"] == k)]},
         "source_hash": source_hash(),
     }
@@ -655,7 +783,7 @@ def run_single(spec: str, reps: int, seed: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--seed", type=int, default=0)

@@ -33,6 +33,20 @@
  *     that nq_last_device_error() reads and clears.
  *   - Thread-safe: no state besides the per-device status word and cached
  *     per-device launch settings.
+ *   - Ordering of weight writes.  The GEMV entry points launch with
+ *     programmatic dependent launch (NQ_PDL=1, the default): the kernel may
+ *     start while the preceding kernel on the stream is still finishing, and
+ *     it reads x only after that kernel has completed, but it starts
+ *     streaming the packed weights and scales at once.  So the packed
+ *     weights and scales must not be written by the kernel launched
+ *     immediately before the GEMV on the same stream.  The library orders its
+ *     own writer: a GEMV that directly follows nq_pack_device on a stream is
+ *     launched without programmatic dependent launch.  A caller that writes
+ *     weights with a kernel of its own (a copy kernel, its own packer) must
+ *     put another launch or a stream-ordered memcpy/event between that kernel
+ *     and the GEMV, or set NQ_PDL=0.  (Weights are read-only in the decode
+ *     loop, where the early start hides the weight stream's start-up latency:
+ *     3 to 6 % per launch, measured.)
  *   - Environment switches, read at each call (for experiments; the defaults
  *     are the measured best): NQ_ROUTE (auto | mma | ffma), NQ_KSPLIT (0 =
  *     the planner's K split, else 1, 2, 4 or 8), NQ_X_F16 (1: fp16 route of
@@ -199,15 +213,39 @@ int nq_gemv_ex(const void* packed, const uint16_t* scales, const void* x_bf16, f
 int nq_gemv_swiglu(const void* packed_gu, const uint16_t* scales_gu, const void* x_bf16,
                    void* act_bf16, int64_t K, int64_t N, int T, int bits, nq_stream_t stream);
 
-/* The decoder layer's MLP on the stream: act = nq_gemv_swiglu(x) then
- * y[T, H_out] = act W_down^T (nq_gemv; the second launch overlaps the first's
- * tail by programmatic dependent launch).  H = K of gate+up, I = intermediate
+/* The decoder layer's MLP on the stream: act = the nq_gemv_swiglu product
+ * of x, then y[T, H_out] = act W_down^T.  H = K of gate+up, I = intermediate
  * size (gate+up has 2 I rows, interleaved as above; down has H_out rows and
  * K = I, a multiple of 64); act_bf16: device scratch [T, I] bf16 owned by the
- * caller (the intermediate, 2 I T bytes). */
+ * caller (the intermediate, 2 I T bytes), written.  The library's choice of
+ * launches (see nq_mlp_ex): two, nq_gemv_swiglu then nq_gemv, the second
+ * overlapping the first's tail by programmatic dependent launch. */
 int nq_mlp(const void* packed_gu, const uint16_t* scales_gu, int bits_gu, const void* packed_down,
            const uint16_t* scales_down, int bits_down, const void* x_bf16, void* act_bf16,
            float* y, int64_t H, int64_t I, int64_t H_out, int T, nq_stream_t stream);
+
+/* nq_mlp with the number of launches chosen by the caller: launches = 0
+ * (the library's choice: 2, or 1 with NQ_MLP_FUSED=1), 1 or 2.  One launch
+ * runs the whole layer in one kernel: its gate+up phase publishes the
+ * activations through a per-device counter, and its down phase starts on
+ * weights the kernel streamed while the gate+up phase finished; the results
+ * equal the two-launch path's bit for bit.  It supports T <= 8, H <= 5120
+ * and the code widths (gate+up, down) = (4, 4), (4, 5), (6, 4), (8, 8)
+ * (nq_mlp_one_launch_ok tells; NQ_EUNSUPPORTED otherwise).  It is measured
+ * 2 to 6 % slower than two launches on GB300, whose clusters of four CTAs
+ * (the down phase's K split) leave 8 of the 152 SMs without work in the
+ * gate+up phase.  One-launch layers whose launches overlap on the GPU in
+ * number beyond 1024 (4096 while capturing graphs) would share counters:
+ * keep fewer layers in flight at once. */
+int nq_mlp_ex(const void* packed_gu, const uint16_t* scales_gu, int bits_gu,
+              const void* packed_down, const uint16_t* scales_down, int bits_down,
+              const void* x_bf16, void* act_bf16, float* y, int64_t H, int64_t I, int64_t H_out,
+              int T, int launches, nq_stream_t stream);
+
+/* Whether nq_mlp_ex(launches = 1) supports this layer shape on the current
+ * device: *ok_out (host) = 1 or 0.  Same shape checks as nq_mlp. */
+int nq_mlp_one_launch_ok(int64_t H, int64_t I, int64_t H_out, int T, int bits_gu, int bits_down,
+                         int* ok_out);
 
 /* Fused verify head: the product of nq_gemv (y may be NULL: logits not
  * stored) and, per token t < T, over the N outputs y[t, 0..N):

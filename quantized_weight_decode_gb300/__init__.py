@@ -19,7 +19,7 @@ import numpy as np
 
 __all__ = [
     "NQError", "ROUTE_AUTO", "ROUTE_MMA", "ROUTE_FFMA", "lib", "lib_path", "build",
-    "packed_bytes", "pack", "pack_gate_up", "unpack", "pack_device", "quantize_rtn", "quantize_search", "gemv", "gemv_swiglu", "mlp", "interleave_gate_up", "gemv_head",
+    "packed_bytes", "pack", "pack_gate_up", "unpack", "pack_device", "quantize_rtn", "quantize_search", "gemv", "gemv_swiglu", "mlp", "mlp_one_launch_ok", "interleave_gate_up", "gemv_head",
     "head_workspace_bytes", "gemv_head_noalloc", "gemv_head_topk", "head_topk_workspace_bytes",
     "dequant",
     "last_device_error", "plan", "selftest_wait_timeout", "status_string", "layout_version",
@@ -49,6 +49,9 @@ _SIGS = {
     "nq_gemv_ex": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp]),
     "nq_gemv_swiglu": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "nq_mlp": (_i32, [_vp, _vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
+    "nq_mlp_ex": (_i32, [_vp, _vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32,
+                         _vp]),
+    "nq_mlp_one_launch_ok": (_i32, [_i64, _i64, _i64, _i32, _i32, _i32, _ip]),
     "nq_gemv_head": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp,
                             ctypes.c_size_t, _vp]),
     "nq_head_workspace_bytes": (_i32, [_szp]),
@@ -260,12 +263,21 @@ def gemv_swiglu(packed_gu, scales_gu, x, act, K: int, N: int, T: int, bits: int,
                                 bits, _stream_handle(stream)), "nq_gemv_swiglu")
 
 
-def mlp(gu, down, x, act, y, T: int, stream=None):
+def mlp(gu, down, x, act, y, T: int, launches: int = 0, stream=None):
     """The layer MLP: gu, down are QuantizedWeight (gu packed interleaved);
-    act [T, I] bf16 scratch, y [T, H_out] fp32."""
-    _check(lib().nq_mlp(_dptr(gu.packed), _dptr(gu.scales), gu.bits, _dptr(down.packed),
-                        _dptr(down.scales), down.bits, _dptr(x), _dptr(act), _dptr(y), gu.K,
-                        gu.N // 2, down.N, T, _stream_handle(stream)), "nq_mlp")
+    act [T, I] bf16 scratch, y [T, H_out] fp32.  launches: 0 = the library's
+    choice, 1 = one launch (nq_mlp_ex), 2 = two launches."""
+    _check(lib().nq_mlp_ex(_dptr(gu.packed), _dptr(gu.scales), gu.bits, _dptr(down.packed),
+                           _dptr(down.scales), down.bits, _dptr(x), _dptr(act), _dptr(y), gu.K,
+                           gu.N // 2, down.N, T, launches, _stream_handle(stream)), "nq_mlp_ex")
+
+
+def mlp_one_launch_ok(H: int, I: int, H_out: int, T: int, bits_gu: int, bits_down: int) -> bool:
+    """Whether nq_mlp_ex(launches=1) supports this layer shape here."""
+    v = ctypes.c_int()
+    _check(lib().nq_mlp_one_launch_ok(H, I, H_out, T, bits_gu, bits_down, ctypes.byref(v)),
+           "nq_mlp_one_launch_ok")
+    return bool(v.value)
 
 
 def head_workspace_bytes() -> int:

@@ -22,6 +22,16 @@ int* device_status_ptr() {
   return static_cast<int*>(p);
 }
 
+// Per device: the activation counters of the one-launch MLP layer, two words
+// per launch slot; zero at load, reset to zero by every launch that uses them.
+__device__ unsigned g_sync_slots[2 * kSyncSlots];
+
+unsigned* sync_slots_ptr() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_sync_slots) != cudaSuccess) return nullptr;
+  return static_cast<unsigned*>(p);
+}
+
 // ------------------------------------------------------------------ packer
 // One thread per (row tile, group, lane): gathers the lane's 32 codes from the
 // row-major code matrix and writes its words; lanes 0..15 also write the

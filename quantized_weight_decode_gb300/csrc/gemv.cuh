@@ -127,7 +127,31 @@ struct GemvArgs {
   int off_tk;
   unsigned long long* tk_lists;
   unsigned long long* tk_bufs;
+  // One-launch MLP layer (nq_mlp_kernel): the gate+up phase's epilogue adds
+  // the number of row tiles whose activations it has stored to sync[0]; the
+  // down phase's consumers wait until sync[0] == sync_target (all of them),
+  // then count themselves in sync[1], and the last CTA to pass resets both
+  // words for the next launch that uses the pair.  Null for a plain GEMV.
+  unsigned* sync;
+  int sync_target;
 };
+
+// Position in the stage ring and the partial-buffer ring, carried from the
+// gate+up phase to the down phase of the one-launch layer.
+struct RingPos {
+  int stage;
+  uint32_t phase;
+  int rb;
+  uint32_t rn;
+};
+// Launch slots of the one-launch layer's activation counters (per device):
+// launches issued while a stream is captured into a CUDA graph take slots of
+// their own pool, so a graph's baked-in slots are never handed to ordinary
+// launches; a slot is reused after kSyncSlotsEager (kSyncSlotsCapture) more
+// launches of its pool.
+constexpr int kSyncSlotsEager = 1024;
+constexpr int kSyncSlotsCapture = 4096;
+constexpr int kSyncSlots = kSyncSlotsEager + kSyncSlotsCapture;
 constexpr int kHeadCounterBytes = 256;
 constexpr int kHeadStateBytes = 16;
 constexpr int kHeadMaxT = 16;
@@ -705,7 +729,7 @@ __device__ __forceinline__ void slice_xr(const uint8_t* codes, const uint8_t* sc
 
 // The lane's x fragments of the warp slice (groups i < n, tokens < T; zeros
 // elsewhere), as bf16 pairs straight from x.
-template <int GWM, int NT>
+template <int GWM, int NT, bool CG = false>
 __device__ __forceinline__ void load_x_frags(const GemvArgs& a, const Slice& sl, int n, int lane,
                                              uint32_t (&xr)[GWM][NT][8]) {
   const int q = lane >> 2, r = lane & 3;
@@ -720,7 +744,9 @@ __device__ __forceinline__ void load_x_frags(const GemvArgs& a, const Slice& sl,
         // the layout's K order: the lane's fragments are x at k = 16r .. 16r + 15
         const uint4* src = reinterpret_cast<const uint4*>(
             a.x + static_cast<long long>(tok) * a.K + 64LL * (sl.gs + i) + 16 * r);
-        const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+        // CG: x was written earlier in the same kernel (the layer's
+        // activations), so it is read through L2, not the read-only path.
+        const uint4 v0 = CG ? __ldcg(src) : __ldg(src), v1 = CG ? __ldcg(src + 1) : __ldg(src + 1);
         xr[i][nb][0] = v0.x; xr[i][nb][1] = v0.y; xr[i][nb][2] = v0.z; xr[i][nb][3] = v0.w;
         xr[i][nb][4] = v1.x; xr[i][nb][5] = v1.y; xr[i][nb][6] = v1.z; xr[i][nb][7] = v1.w;
       }
@@ -822,10 +848,11 @@ __device__ inline bool stage_x_f16(const GemvArgs& a, uint8_t* smem, const Work&
 // hand the partials over at once.
 // F16: fp16 route; the partials are brought back to the scale of x (inv) and
 // rows q + 8 divided by 16 before they are handed over.
-template <int BITS, int GWM, int NT, bool F16, int NG>
+template <int BITS, int GWM, int NT, bool F16, int NG, bool CONT = false>
 __device__ void xreg_jobs(const GemvArgs& a, uint8_t* smem, const Bars& bars, const Waiter& wt,
                           const Work& wk, int warp, int lane, int codes_off, int scales_off,
-                          const uint32_t (&xr)[GWM][NT][8], const float (&inv)[NT][2]) {
+                          const uint32_t (&xr)[GWM][NT][8], const float (&inv)[NT][2],
+                          RingPos* pos = nullptr) {
   constexpr int JT = NT == 1 ? 2 : 1;   // = kJobTiles of the kernel
   const int q = lane >> 2;
   const uint8_t* ring = smem + a.off_ring;
@@ -839,6 +866,12 @@ __device__ void xreg_jobs(const GemvArgs& a, uint8_t* smem, const Bars& bars, co
   uint32_t phase = 0;
   int rb = 0;        // partial buffer of this pair
   uint32_t rn = 0;   // uses of that buffer so far
+  if constexpr (CONT) {  // continue where the previous phase left the rings
+    stage = pos->stage;
+    phase = pos->phase;
+    rb = pos->rb;
+    rn = pos->rn;
+  }
   for (int j = 0; j < wk.njobs; j += JT) {
     float acc[JT][NT][4];
 #pragma unroll
@@ -870,21 +903,23 @@ __device__ void xreg_jobs(const GemvArgs& a, uint8_t* smem, const Bars& bars, co
     if (!hand_partials_mma<NT, JT>(a, smem, bars, wt, warp, lane, rb, rn, acc)) return;
     if (++rb == a.nbuf) { rb = 0; ++rn; }
   }
+  if constexpr (CONT) *pos = RingPos{stage, phase, rb, rn};
 }
 
 // The slice length n (uniform per warp, <= GWM) picks the job loop once.
-template <int BITS, int GWM, int NT, bool F16>
+template <int BITS, int GWM, int NT, bool F16, bool CONT = false>
 __device__ __forceinline__ void run_xreg_jobs(const GemvArgs& a, uint8_t* smem, const Bars& bars,
                                               const Waiter& wt, const Work& wk, int warp,
                                               int lane, int n, int codes_off, int scales_off,
                                               const uint32_t (&xr)[GWM][NT][8],
-                                              const float (&inv)[NT][2]) {
+                                              const float (&inv)[NT][2],
+                                              RingPos* pos = nullptr) {
   static_assert(GWM <= 5, "slice-length dispatch covers 1..5 groups");
 #define NQ_XREG_CASE(k)                                                                      \
   case k:                                                                                    \
     if constexpr (k <= GWM)                                                                  \
-      xreg_jobs<BITS, GWM, NT, F16, k>(a, smem, bars, wt, wk, warp, lane, codes_off,         \
-                                       scales_off, xr, inv);                                 \
+      xreg_jobs<BITS, GWM, NT, F16, k, CONT>(a, smem, bars, wt, wk, warp, lane, codes_off,   \
+                                             scales_off, xr, inv, pos);                      \
     break;
   switch (n) {
     NQ_XREG_CASE(1)
@@ -894,8 +929,8 @@ __device__ __forceinline__ void run_xreg_jobs(const GemvArgs& a, uint8_t* smem, 
     NQ_XREG_CASE(5)
     default:
       // A warp without groups still takes part in every hand-off (zeros).
-      xreg_jobs<BITS, GWM, NT, F16, 0>(a, smem, bars, wt, wk, warp, lane, codes_off, scales_off,
-                                       xr, inv);
+      xreg_jobs<BITS, GWM, NT, F16, 0, CONT>(a, smem, bars, wt, wk, warp, lane, codes_off,
+                                             scales_off, xr, inv, pos);
       break;
   }
 #undef NQ_XREG_CASE
@@ -905,9 +940,10 @@ __device__ __forceinline__ void run_xreg_jobs(const GemvArgs& a, uint8_t* smem, 
 // decodes its fixed slice of it (at most GWM groups) against x fragments of
 // NT token blocks loaded once per kernel.  4-bit codes take the fp16 route
 // when x converts exactly (see stage_x_f16), every other case the bf16 route.
-template <int BITS, int GWM, int NT>
+template <int BITS, int GWM, int NT, bool CONT = false>
 __device__ void consumer_xreg(const GemvArgs& a, uint8_t* smem, const Bars& bars,
-                              const Waiter& wt, const Work& wk, int warp, int lane) {
+                              const Waiter& wt, const Work& wk, int warp, int lane,
+                              RingPos* pos = nullptr) {
   constexpr int kBlock = 128 * BITS;
   const Slice sl = warp_slice(wk, warp);
   const int n = sl.ge - sl.gs;  // <= GWM
@@ -952,22 +988,23 @@ __device__ void consumer_xreg(const GemvArgs& a, uint8_t* smem, const Bars& bars
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(smem + kXFreeBarOffset));
       if (f16) {
-        run_xreg_jobs<BITS, GWM, NT, true>(a, smem, bars, wt, wk, warp, lane, n, codes_off,
-                                       scales_off, xr, inv);
+        run_xreg_jobs<BITS, GWM, NT, true, CONT>(a, smem, bars, wt, wk, warp, lane, n, codes_off,
+                                                 scales_off, xr, inv, pos);
         return;
       }
 #pragma unroll
       for (int nb = 0; nb < NT; ++nb) inv[nb][0] = inv[nb][1] = 1.f;
-      run_xreg_jobs<BITS, GWM, NT, false>(a, smem, bars, wt, wk, warp, lane, n, codes_off, scales_off,
-                                      xr, inv);
+      run_xreg_jobs<BITS, GWM, NT, false, CONT>(a, smem, bars, wt, wk, warp, lane, n, codes_off,
+                                                scales_off, xr, inv, pos);
       return;
     }
   }
-  load_x_frags<GWM, NT>(a, sl, n, lane, xr);
+  // (A continuing phase reads x that this kernel wrote: through L2.)
+  load_x_frags<GWM, NT, CONT>(a, sl, n, lane, xr);
 #pragma unroll
   for (int nb = 0; nb < NT; ++nb) inv[nb][0] = inv[nb][1] = 1.f;
-  run_xreg_jobs<BITS, GWM, NT, false>(a, smem, bars, wt, wk, warp, lane, n, codes_off, scales_off, xr,
-                                  inv);
+  run_xreg_jobs<BITS, GWM, NT, false, CONT>(a, smem, bars, wt, wk, warp, lane, n, codes_off,
+                                            scales_off, xr, inv, pos);
 }
 
 // x in shared memory: the warps take the groups of each stage in turn
@@ -1288,9 +1325,12 @@ __device__ __forceinline__ void topk_update(const GemvArgs& a, unsigned long lon
   }
 }
 
-template <int SLOTS, int JT>
+// CONT: a phase of the one-launch layer; its hand-offs continue the CTA's
+// sequence after `h0` hand-offs of the previous phase (hand-off g uses
+// buffer g % nbuf and belongs to epilogue warp g % kEpiWarps).
+template <int SLOTS, int JT, bool CONT = false>
 __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& bars,
-                                const Waiter& wt, const Work& wk, int ew, int lane) {
+                                const Waiter& wt, const Work& wk, int ew, int lane, int h0 = 0) {
   const int T = a.T;
   const int nvt = 16 * T;            // values per row tile (a multiple of 16)
   const int nv = JT * nvt;           // values per hand-off (JT consecutive tiles)
@@ -1334,9 +1374,20 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
   }
   int b = ew;        // buffer of hand-off j (j % nbuf)
   uint32_t n = 0;    // uses of that buffer so far (j / nbuf)
-  for (int j = ew; j < njt; j += kEpiWarps) {
+  int j = ew;
+  if constexpr (CONT) {
+    j = (ew - h0 % kEpiWarps + kEpiWarps) % kEpiWarps;  // first local hand-off of this warp
+    b = (h0 + j) % a.nbuf;
+    n = static_cast<uint32_t>((h0 + j) / a.nbuf);
+  }
+  for (; j < njt; j += kEpiWarps) {
+    // Cluster-exchange buffer of this hand-off: its position among this
+    // launch's K-split hand-offs, the same on every rank (a continuing phase
+    // starts its own count; its red buffers continue the CTA's count).
+    const int cb = CONT ? j % a.nbuf : b;
+    const uint32_t cn = CONT ? static_cast<uint32_t>(j / a.nbuf) : n;
     if (ks > 1 && wk.rank == 0 && lane == 0)
-      mbar_arrive_expect_tx_relaxed(bars.cl_full(b), cl_bytes);
+      mbar_arrive_expect_tx_relaxed(bars.cl_full(cb), cl_bytes);
     if (!wt.wait_warp<false>(bars.red_full(b), n & 1u)) return;
     float4 v[SLOTS];
 #pragma unroll
@@ -1354,25 +1405,25 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
     bool store = true;
     if (ks > 1) {
       if (wk.rank != 0) {
-        if (!wt.wait_warp<false>(bars.cl_empty(b), (n & 1u) ^ 1u)) return;
+        if (!wt.wait_warp<false>(bars.cl_empty(cb), (cn & 1u) ^ 1u)) return;
         const uint32_t dst0 =
-            map_to_rank(smem_addr(cl + (b * (ks - 1) + (wk.rank - 1)) * nv + 4 * lane), 0);
-        const uint32_t bar0 = map_to_rank(bars.cl_full(b), 0);
+            map_to_rank(smem_addr(cl + (cb * (ks - 1) + (wk.rank - 1)) * nv + 4 * lane), 0);
+        const uint32_t bar0 = map_to_rank(bars.cl_full(cb), 0);
 #pragma unroll
         for (int i = 0; i < SLOTS; ++i)
           if (has(i)) st_async_v4(dst0 + 512 * i, v[i], bar0);
         store = false;
       } else {
-        if (!wt.wait_warp<false>(bars.cl_full(b), n & 1u)) return;
+        if (!wt.wait_warp<false>(bars.cl_full(cb), cn & 1u)) return;
         for (int p = 1; p < ks; ++p) {
-          const float* src = cl + (b * (ks - 1) + (p - 1)) * nv + 4 * lane;
+          const float* src = cl + (cb * (ks - 1) + (p - 1)) * nv + 4 * lane;
 #pragma unroll
           for (int i = 0; i < SLOTS; ++i)
             if (has(i)) add4(v[i], *reinterpret_cast<const float4*>(src + 128 * i));
         }
         __syncwarp();
         if (lane == 0) {
-          for (int p = 1; p < ks; ++p) mbar_arrive_remote_relaxed(map_to_rank(bars.cl_empty(b), p));
+          for (int p = 1; p < ks; ++p) mbar_arrive_remote_relaxed(map_to_rank(bars.cl_empty(cb), p));
         }
       }
     }
@@ -1396,6 +1447,13 @@ __device__ inline void epilogue(const GemvArgs& a, uint8_t* smem, const Bars& ba
           pk.y = *reinterpret_cast<const uint32_t*>(&hi);
           *reinterpret_cast<uint2*>(a.act + vtok[i] * ni + idx) = pk;
         }
+      }
+      if (a.sync != nullptr) {
+        // One-launch layer: publish this hand-off's activations (every
+        // lane's stores, then one count) to the down phase's consumers.
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(a.sync, static_cast<unsigned>(min(JT, wk.njobs - j * JT)));
       }
     } else if (store) {
 #pragma unroll
@@ -1509,6 +1567,154 @@ __global__ void __launch_bounds__(kThreads, 1) nq_gemv_kernel(const __grid_const
   // memory or arrive on its barriers.
   __syncwarp();
   if (a.ksplit > 1) cluster_sync_all();
+}
+
+// ------------------------------------------------------------------ one-launch MLP layer
+// The decoder layer's MLP in one launch (pages "giveen/ninfer-ext", section
+// "Where ninfer-ext leads", and "Qwen3.8-27B for NInfer on the RTX 3090",
+// section "What is different from the upstream artifact": gate and up as one
+// matrix, then the down projection).  Phase A is the gate+up product with the
+// SwiGLU epilogue, every CTA working alone (no K split); phase B is the down
+// projection over the activations phase A wrote, in clusters of b.ksplit.
+// Both phases share the stage ring and the partial-buffer ring, so the
+// producer streams phase B's weights while phase A finishes, and phase B's
+// consumers start on full stages once every activation is published.
+
+// Issues the bulk copies of one phase's jobs (the loop body of producer()).
+template <int BITS>
+__device__ __forceinline__ bool producer_phase(const GemvArgs& a, uint8_t* smem, const Bars& bars,
+                                               const Waiter& wt, const Work& wk, uint64_t policy,
+                                               int& stage, uint32_t& phase, uint32_t& issued,
+                                               uint32_t& last_par, bool& x_pending) {
+  constexpr int kBlock = 128 * BITS;
+  const uint32_t ring = smem_addr(smem + a.off_ring);
+  const int sg = a.stage_groups;
+  for (int j = 0; j < wk.njobs; ++j) {
+    const long long blk_job = (wk.rt_begin + j) * a.G;
+    for (int g0 = wk.g_begin; g0 < wk.g_end; g0 += sg) {
+      const int ng = min(sg, wk.g_end - g0);
+      if (!wt.wait<false>(bars.empty(stage), phase ^ 1)) return false;
+      if (x_pending && stage >= a.xh_stage0) {
+        if (!wt.wait<false>(smem_addr(smem + kXFreeBarOffset), 0)) return false;
+        fence_proxy_async_smem();
+        x_pending = false;
+      }
+      const uint32_t bc = static_cast<uint32_t>(ng * kBlock);
+      const uint32_t bs = static_cast<uint32_t>(ng * kScaleBytesPerBlock);
+      const uint32_t dst = ring + stage * a.stage_bytes;
+      const long long blk = blk_job + g0;
+      mbar_arrive_expect_tx(bars.full(stage), bc + bs);
+      bulk_g2s(dst, a.codes + blk * kBlock, bc, bars.full(stage), policy);
+      bulk_g2s(dst + sg * kBlock, a.scales + blk * 16, bs, bars.full(stage), policy);
+      issued |= 1u << stage;
+      last_par = (last_par & ~(1u << stage)) | (phase << stage);
+      if (++stage == a.stages) { stage = 0; phase ^= 1; }
+    }
+  }
+  return true;
+}
+
+template <int BITS_A, int BITS_B>
+__device__ void producer_layer(const GemvArgs& a, const GemvArgs& b, uint8_t* smem, const Bars& bars,
+                               const Waiter& wt, const Work& wa, const Work& wb) {
+  const uint64_t policy = l2_evict_first_policy();
+  int stage = 0;
+  uint32_t phase = 0, issued = 0, last_par = 0;
+  bool x_pending = a.off_xh >= 0;
+  if (producer_phase<BITS_A>(a, smem, bars, wt, wa, policy, stage, phase, issued, last_par, x_pending))
+    (void)producer_phase<BITS_B>(b, smem, bars, wt, wb, policy, stage, phase, issued, last_par,
+                                 x_pending);
+  volatile int no_abort = 0;
+  const Waiter drain{&no_abort, wt.limit, wt.status};
+  for (int s = 0; s < a.stages; ++s)
+    if (issued & (1u << s)) (void)drain.wait<false>(bars.full(s), (last_par >> s) & 1u);
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Consumer warps: wait until every activation of phase A is published.  Warp
+// 0 polls (bounded); the others wait at a barrier of the consumer warps.
+// The last CTA to pass resets the pair for the next launch that uses it.
+__device__ __forceinline__ bool wait_activations(const GemvArgs& b, const Waiter& wt, int warp,
+                                                 int lane) {
+  if (warp == 0 && lane == 0) {
+    const uint64_t t0 = global_ns();
+    while (ld_acquire_gpu(b.sync) < static_cast<unsigned>(b.sync_target)) {
+      if (*wt.abort) break;
+      if (global_ns() - t0 > wt.limit) {
+        *wt.abort = 1;
+        atomicCAS(wt.status, 0, kStatusTimeout);
+        break;
+      }
+      __nanosleep(32);
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+  if (*wt.abort) return false;
+  (void)ld_acquire_gpu(b.sync);  // orders this lane's loads of the activations
+  if (warp == 0 && lane == 0 && atomicAdd(b.sync + 1, 1u) == gridDim.x - 1) {
+    atomicExch(b.sync, 0u);
+    atomicExch(b.sync + 1, 0u);
+  }
+  return true;
+}
+
+template <int BITS_A, int BITS_B>
+__global__ void __launch_bounds__(kThreads, 1)
+    nq_mlp_kernel(const __grid_constant__ GemvArgs a, const __grid_constant__ GemvArgs b) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Bars bars{smem_addr(smem)};
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortFlagOffset);
+  const Waiter wt{abort_flag, a.wait_ns, a.status};
+  const Work wa = cta_work(a);  // phase A: every CTA alone (a.ksplit == 1)
+  const Work wb = cta_work(b);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(bars.full(s), 1);
+      mbar_init(bars.empty(s), kWarps);
+    }
+    for (int i = 0; i < a.nbuf; ++i) {
+      mbar_init(bars.red_full(i), 32 * kWarps);
+      mbar_init(bars.red_empty(i), 32);
+      mbar_init(bars.cl_full(i), 1);
+      mbar_init(bars.cl_empty(i), 1);
+    }
+    *abort_flag = 0;
+    for (int i = 0; i < 8; ++i) reinterpret_cast<uint32_t*>(smem + kZeroAreaOffset)[i] = 0u;
+    mbar_init(smem_addr(smem + kXFreeBarOffset), kWarps);
+    uint32_t* stat = reinterpret_cast<uint32_t*>(smem + kXStatOffset);
+    for (int t = 0; t < 16; ++t) {
+      stat[t] = 0u;
+      stat[16 + t] = 0x7FFFu;
+    }
+    stat[32] = 0u;
+    fence_mbar_init();
+  }
+  griddep_launch_dependents();
+  if (b.ksplit > 1) cluster_sync_all(); else __syncthreads();
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) producer_layer<BITS_A, BITS_B>(a, b, smem, bars, wt, wa, wb);
+  } else if (warp >= kEpilogueWarp) {
+    const int ew = warp - kEpilogueWarp;
+    griddep_wait();
+    epilogue<2, 2, true>(a, smem, bars, wt, wa, ew, lane, 0);
+    epilogue<2, 2, true>(b, smem, bars, wt, wb, ew, lane, (wa.njobs + 1) / 2);
+  } else {
+    griddep_wait();
+    RingPos pos{0, 0u, 0, 0u};
+    consumer_xreg<BITS_A, kXregMaxGroups, 1, true>(a, smem, bars, wt, wa, warp, lane, &pos);
+    if (wait_activations(b, wt, warp, lane))
+      consumer_xreg<BITS_B, kXregMaxGroups, 1, true>(b, smem, bars, wt, wb, warp, lane, &pos);
+  }
+  __syncwarp();
+  if (b.ksplit > 1) cluster_sync_all();
 }
 
 }  // namespace nq

@@ -9,6 +9,7 @@
 #include <cstdlib>
 #include <climits>
 #include <cstring>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -34,6 +35,8 @@ cudaError_t launch_selftest_timeout(unsigned long long, int*, cudaStream_t);
 cudaError_t launch_topk_merge(const unsigned long long*, int, int, int, int32_t*, float*, bool,
                               cudaStream_t);
 int* device_status_ptr();
+unsigned* sync_slots_ptr();
+const void* mlp_kernel(int bits_gu, int bits_down);
 
 namespace {
 
@@ -46,12 +49,34 @@ struct DevInfo {
   int sms = 0;
   int smem_optin = 0;
   int* status = nullptr;
+  unsigned* sync = nullptr;  // activation counters of the one-launch layer (kSyncSlots pairs)
 };
 
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
 std::map<std::tuple<int, const void*>, bool> g_func_ready;
 std::map<std::tuple<int, const void*, int, int>, int> g_clusters;
+// Streams whose last launch by this library wrote packed weights
+// (nq_pack_device): the next GEMV on such a stream is launched without
+// programmatic dependent launch, because the GEMV's producer starts reading
+// weights before it waits for the preceding kernel.
+std::map<cudaStream_t, bool> g_weights_written;
+std::atomic<unsigned> g_sync_eager{0};
+std::atomic<unsigned> g_sync_capture{0};
+
+void mark_weights_written(cudaStream_t st) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_weights_written[st] = true;
+}
+// True if the preceding launch of this library on `st` wrote packed weights
+// (and forgets it: the GEMV about to launch orders everything after it).
+bool take_weights_written(cudaStream_t st) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_weights_written.find(st);
+  if (it == g_weights_written.end() || !it->second) return false;
+  it->second = false;
+  return true;
+}
 
 int current_device(int* dev) {
   if (cudaGetDevice(dev) != cudaSuccess) {
@@ -75,7 +100,8 @@ int dev_info(DevInfo** out) {
       return NQ_ECUDA;
     }
     d.status = device_status_ptr();
-    if (!d.status) {
+    d.sync = sync_slots_ptr();
+    if (!d.status || !d.sync) {
       (void)cudaGetLastError();
       return NQ_ECUDA;
     }
@@ -393,7 +419,7 @@ int launch_plan(const Plan& p, const void* packed, const uint16_t* scales, const
                 uint16_t* act = nullptr) {
   DevInfo* d;
   if (int rc = dev_info(&d)) return rc;
-  GemvArgs a;
+  GemvArgs a = {};  // every field not set below is zero (null sync: a plain product)
   a.codes = static_cast<const uint8_t*>(packed);
   a.scales = scales;
   a.x = static_cast<const uint16_t*>(x);
@@ -441,7 +467,8 @@ int launch_plan(const Plan& p, const void* packed, const uint16_t* scales, const
     at[na].val.clusterDim.z = 1;
     ++na;
   }
-  if (env_int("NQ_PDL", 1) != 0) {
+  const bool after_pack = take_weights_written(st);
+  if (env_int("NQ_PDL", 1) != 0 && !after_pack) {
     at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
@@ -449,6 +476,184 @@ int launch_plan(const Plan& p, const void* packed, const uint16_t* scales, const
   cfg.attrs = at;
   cfg.numAttrs = na;
   void* args[] = {&a};
+  if (cudaLaunchKernelExC(&cfg, p.func, args) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return NQ_ECUDA;
+  }
+  return NQ_OK;
+}
+
+// ---------------------------------------------------------------- one-launch MLP layer
+struct MlpPlan {
+  Plan p;                // shared layout: ring, partial buffers, fp16 staging of phase A
+  int ks = 1;            // K split of the down phase (cluster size)
+  int sg_a = 0, sg_b = 0;
+};
+
+// The layer runs in one launch when both phases fit the x-in-register kernel
+// with one token block (T <= 8): the gate+up phase without a K split (at
+// most 5 x 16 groups of K), the down phase at the K split nq_gemv would use.
+// Anything else is NQ_EUNSUPPORTED, and nq_mlp takes two launches.
+int make_mlp_plan(int64_t H, int64_t I, int64_t H_out, int T, int bits_gu, int bits_down,
+                  MlpPlan* out) {
+  if (T < 1 || T > 8) return NQ_EUNSUPPORTED;
+  const void* func = mlp_kernel(bits_gu, bits_down);
+  if (!func) return NQ_EUNSUPPORTED;
+  if (int rc = check_shape(H, 2 * I, bits_gu)) return rc;
+  if (int rc = check_shape(I, H_out, bits_down)) return rc;
+  const int G_a = static_cast<int>(H / kGroup);
+  if ((G_a + kWarps - 1) / kWarps > kXregMaxGroups) return NQ_EUNSUPPORTED;
+  Plan pb;
+  if (int rc = make_plan(I, H_out, T, bits_down, NQ_ROUTE_MMA, 0, &pb)) return rc;
+  if (pb.ntok != kNtokXreg) return NQ_EUNSUPPORTED;
+  DevInfo* d;
+  if (int rc = dev_info(&d)) return rc;
+  int dev;
+  if (int rc = current_device(&dev)) return rc;
+  if (int rc = prepare_func(dev, func, d->smem_optin)) return rc;
+  const int ks = pb.ks;
+  const int G_b = static_cast<int>(I / kGroup);
+  const int gc_b = (G_b + ks - 1) / ks;
+  const int sb_a = align_up(G_a * (block_bytes(bits_gu) + kScaleBytesPerBlock), 128);
+  const int sb_b = align_up(gc_b * (block_bytes(bits_down) + kScaleBytesPerBlock), 128);
+  const int stage_bytes = std::max(sb_a, sb_b);
+  // Partial buffers as layout_for() sets them for the pair-of-tiles kernel:
+  // the deep count where three ring stages remain, else the standard one.
+  const int std_nbuf = T <= 2 ? 4 : 2, deep_nbuf = T <= 4 ? kMaxBufs : 4;
+  Plan p;
+  bool fit = false;
+  for (int nbuf : {deep_nbuf, std_nbuf}) {
+    const int red_bytes = nbuf * kWarps * 2 * 16 * T * 4;
+    const int cl_bytes = ks > 1 ? nbuf * (ks - 1) * 2 * 16 * T * 4 : 0;
+    p = Plan();
+    p.route = NQ_ROUTE_MMA;
+    p.ntok = kNtokXreg;
+    p.ks = ks;
+    p.nbuf = nbuf;
+    p.stage_bytes = stage_bytes;
+    p.off_red = kBarRegionBytes;
+    p.off_cl = p.off_red + align_up(red_bytes, 128);
+    p.off_x = p.off_cl + align_up(cl_bytes, 128);
+    p.off_tk = p.off_x;
+    p.off_ring = p.off_x;
+    p.stages = std::min(kMaxStages, (d->smem_optin - p.off_ring) / stage_bytes);
+    const int min_stages = (nbuf == deep_nbuf && deep_nbuf > std_nbuf) ? 3 : 2;
+    if (p.stages >= min_stages) {
+      fit = true;
+      break;
+    }
+  }
+  if (!fit) return NQ_EUNSUPPORTED;
+  p.smem = p.off_ring + p.stages * stage_bytes;
+  // Phase A's fp16 staging of x (4-bit gate+up, T <= 2) at the ring's tail,
+  // as for the single product.
+  p.off_xh = -1;
+  p.xh_stage0 = p.stages;
+  if (bits_gu == 4 && T <= kF16MaxT && env_int("NQ_X_F16", 1) != 0) {
+    const int xh_bytes = align_up(G_a * T * 128, 128);
+    const int off = (p.smem - xh_bytes) / 128 * 128;
+    if (off >= p.off_ring + stage_bytes) {
+      p.off_xh = off;
+      p.xh_stage0 = (off - p.off_ring) / stage_bytes;
+    }
+  }
+  p.func = func;
+  const int mc = max_clusters(dev, *d, func, ks, p.smem);
+  if (mc <= 0) return NQ_EUNSUPPORTED;
+  p.clusters = mc;
+  out->p = p;
+  out->ks = ks;
+  out->sg_a = G_a;
+  out->sg_b = gc_b;
+  return NQ_OK;
+}
+
+int launch_mlp(const MlpPlan& mp, const void* packed_gu, const uint16_t* scales_gu,
+               const void* packed_down, const uint16_t* scales_down, const void* x, void* act,
+               float* y, int64_t H, int64_t I, int64_t H_out, int T, cudaStream_t st) {
+  DevInfo* d;
+  if (int rc = dev_info(&d)) return rc;
+  const Plan& p = mp.p;
+  // This launch's activation counters: a slot of the eager pool, or of the
+  // capture pool while the stream is being captured into a graph.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+    (void)cudaGetLastError();
+    cs = cudaStreamCaptureStatusNone;
+  }
+  const unsigned slot = cs == cudaStreamCaptureStatusActive
+                            ? kSyncSlotsEager + g_sync_capture.fetch_add(1) % kSyncSlotsCapture
+                            : g_sync_eager.fetch_add(1) % kSyncSlotsEager;
+  GemvArgs a = {};
+  a.codes = static_cast<const uint8_t*>(packed_gu);
+  a.scales = scales_gu;
+  a.x = static_cast<const uint16_t*>(x);
+  a.y = nullptr;
+  a.act = static_cast<uint16_t*>(act);
+  a.N = 2 * I;
+  a.K = static_cast<int>(H);
+  a.T = T;
+  a.G = static_cast<int>(H / kGroup);
+  a.Nt = static_cast<int>((2 * I + kTileRows - 1) / kTileRows);
+  a.ksplit = 1;                     // every CTA alone
+  a.clusters = p.clusters * mp.ks;  // = CTAs
+  a.stage_groups = mp.sg_a;
+  a.stages = p.stages;
+  a.stage_bytes = p.stage_bytes;
+  a.off_ring = p.off_ring;
+  a.off_red = p.off_red;
+  a.off_cl = p.off_cl;
+  a.off_x = p.off_x;
+  a.off_xh = p.off_xh;
+  a.xh_stage0 = p.xh_stage0;
+  a.nbuf = p.nbuf;
+  a.wait_ns = static_cast<unsigned long long>(std::max(1, env_int("NQ_WAIT_MS", 2000))) * 1000000ULL;
+  a.status = d->status;
+  a.sync = d->sync + 2 * static_cast<size_t>(slot);
+  a.sync_target = 0;
+  GemvArgs b = a;
+  b.codes = static_cast<const uint8_t*>(packed_down);
+  b.scales = scales_down;
+  b.x = static_cast<const uint16_t*>(act);
+  b.y = y;
+  b.act = nullptr;
+  b.N = H_out;
+  b.K = static_cast<int>(I);
+  b.G = static_cast<int>(I / kGroup);
+  b.Nt = static_cast<int>((H_out + kTileRows - 1) / kTileRows);
+  b.ksplit = mp.ks;
+  b.clusters = p.clusters;
+  b.stage_groups = mp.sg_b;
+  // Phase B has no fp16 staging of its own, but its first fills of the stages
+  // that overlap phase A's staging area must still wait until phase A's
+  // consumers have taken their x (the producer's check uses xh_stage0).
+  b.off_xh = -1;
+  b.xh_stage0 = p.xh_stage0;
+  b.sync_target = a.Nt;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.clusters * mp.ks));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(p.smem);
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  int na = 0;
+  if (mp.ks > 1) {
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = mp.ks;
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  const bool after_pack = take_weights_written(st);
+  if (env_int("NQ_PDL", 1) != 0 && !after_pack) {
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = na;
+  void* args[] = {&a, &b};
   if (cudaLaunchKernelExC(&cfg, p.func, args) != cudaSuccess) {
     (void)cudaGetLastError();
     return NQ_ECUDA;
@@ -639,6 +844,7 @@ int nq_pack_device(const int8_t* codes, const uint16_t* scales, int64_t K, int64
     (void)cudaGetLastError();
     return NQ_ECUDA;
   }
+  mark_weights_written(reinterpret_cast<cudaStream_t>(stream));
   return NQ_OK;
 }
 
@@ -840,16 +1046,51 @@ int nq_gemv_swiglu(const void* packed_gu, const uint16_t* scales_gu, const void*
                      static_cast<uint16_t*>(act_bf16));
 }
 
-int nq_mlp(const void* packed_gu, const uint16_t* scales_gu, int bits_gu, const void* packed_down,
-           const uint16_t* scales_down, int bits_down, const void* x_bf16, void* act_bf16,
-           float* y, int64_t H, int64_t I, int64_t H_out, int T, nq_stream_t stream) {
+int nq_mlp_ex(const void* packed_gu, const uint16_t* scales_gu, int bits_gu,
+              const void* packed_down, const uint16_t* scales_down, int bits_down,
+              const void* x_bf16, void* act_bf16, float* y, int64_t H, int64_t I, int64_t H_out,
+              int T, int launches, nq_stream_t stream) {
   if (!packed_down || !scales_down || !y) return NQ_EINVAL;
   if (I <= 0 || I % 64 != 0) return NQ_EINVAL;
+  if (launches < 0 || launches > 2) return NQ_EINVAL;
   if (int rc = check_shape(I, H_out, bits_down)) return rc;
   if (!aligned16(packed_down) || !aligned16(scales_down) || !aligned16(y)) return NQ_EALIGN;
+  if (!packed_gu || !scales_gu || !x_bf16 || !act_bf16) return NQ_EINVAL;
+  if (int rc = check_shape(H, 2 * I, bits_gu)) return rc;
+  if (T < 1 || T > kMaxT) return NQ_EINVAL;
+  if (!aligned16(packed_gu) || !aligned16(scales_gu) || !aligned16(x_bf16) || !aligned16(act_bf16))
+    return NQ_EALIGN;
+  // The library's choice is two launches: measured faster on GB300 (the
+  // one-launch kernel runs its gate+up phase on the down phase's clusters of
+  // four, which leave 8 of the 152 SMs idle).  NQ_MLP_FUSED=1 changes it.
+  if (launches == 0) launches = env_int("NQ_MLP_FUSED", 0) != 0 ? 1 : 2;
+  if (launches == 1) {
+    MlpPlan mp;
+    if (int rc = make_mlp_plan(H, I, H_out, T, bits_gu, bits_down, &mp)) return rc;
+    return launch_mlp(mp, packed_gu, scales_gu, packed_down, scales_down, x_bf16, act_bf16, y, H,
+                      I, H_out, T, reinterpret_cast<cudaStream_t>(stream));
+  }
   if (int rc = nq_gemv_swiglu(packed_gu, scales_gu, x_bf16, act_bf16, H, 2 * I, T, bits_gu, stream))
     return rc;
   return nq_gemv(packed_down, scales_down, act_bf16, y, I, H_out, T, bits_down, stream);
+}
+
+int nq_mlp(const void* packed_gu, const uint16_t* scales_gu, int bits_gu, const void* packed_down,
+           const uint16_t* scales_down, int bits_down, const void* x_bf16, void* act_bf16,
+           float* y, int64_t H, int64_t I, int64_t H_out, int T, nq_stream_t stream) {
+  return nq_mlp_ex(packed_gu, scales_gu, bits_gu, packed_down, scales_down, bits_down, x_bf16,
+                   act_bf16, y, H, I, H_out, T, 0, stream);
+}
+
+int nq_mlp_one_launch_ok(int64_t H, int64_t I, int64_t H_out, int T, int bits_gu, int bits_down,
+                         int* ok_out) {
+  if (!ok_out) return NQ_EINVAL;
+  if (I <= 0 || I % 64 != 0 || T < 1 || T > kMaxT) return NQ_EINVAL;
+  if (int rc = check_shape(H, 2 * I, bits_gu)) return rc;
+  if (int rc = check_shape(I, H_out, bits_down)) return rc;
+  MlpPlan mp;
+  *ok_out = make_mlp_plan(H, I, H_out, T, bits_gu, bits_down, &mp) == NQ_OK ? 1 : 0;
+  return NQ_OK;
 }
 
 int nq_gemv_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, int* route_out,
@@ -888,6 +1129,12 @@ int nq_last_device_error(nq_stream_t stream) {
   const int zero = 0;
   if (cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
       cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return NQ_ECUDA;
+  }
+  // A layer that gave up on a bounded wait may have left its activation
+  // counters behind: clear every slot (nothing of this device may run).
+  if (v != 0 && cudaMemset(d->sync, 0, 2 * sizeof(unsigned) * kSyncSlots) != cudaSuccess) {
     (void)cudaGetLastError();
     return NQ_ECUDA;
   }

@@ -59,11 +59,18 @@ def _gate_up_case(tag, bits, I, H, T):
 def _check_act(act_bits, cg, sg, cu, su, xb, cd=None, sd=None):
     """act against oracle.mlp (gate+up in (gate; up) row order); with down
     weights, also returns the oracle's layer output and its error scale."""
-    if cd is None:                      # no down product: a zero matrix of K = I
-        cd = np.zeros((16, cg.shape[0]), np.int8)
-        sd = np.zeros((16, cg.shape[0] // 64), np.uint16)
+    I = cg.shape[0]
+    if cd is None:
+        # no down product: zero rows pad gate and up to a multiple of 64 (their
+        # activations are 0) and a zero down matrix takes the padded act
+        pad = -I % 64
+        z = lambda a: np.concatenate([a, np.zeros((pad,) + a.shape[1:], a.dtype)])
+        cg, sg, cu, su = z(cg), z(sg), z(cu), z(su)
+        cd = np.zeros((16, I + pad), np.int8)
+        sd = np.zeros((16, (I + pad) // 64), np.uint16)
     act_ref, y_ref, e_ref, g, u, e_g, e_u = oracle.mlp(
         np.concatenate([cg, cu]), np.concatenate([sg, su]), cd, sd, xb)
+    act_ref, g, u, e_g, e_u = (a[:, :I] for a in (act_ref, g, u, e_g, e_u))
     ref = oracle.bf16_to_f64(act_ref)
     got = oracle.bf16_to_f64(act_bits)
     tol = _act_tolerance(g, u, e_g, e_u)
@@ -91,7 +98,7 @@ def test_swiglu_rejects_ragged_rows():
     assert e.value.code == nqp.EINVAL
 
 
-def _check_layer(I, H, Hout, bits_gu, bits_down, T, tag):
+def _check_layer(I, H, Hout, bits_gu, bits_down, T, tag, launches=None):
     cg, sg, cu, su, xb, packed, sp = _gate_up_case(tag, bits_gu, I, H, T)
     rng = synth.generator(0, *tag, 9)
     wd = synth.gauss_weights(rng, Hout, I)
@@ -102,13 +109,16 @@ def _check_layer(I, H, Hout, bits_gu, bits_down, T, tag):
     x = torch.from_numpy(xb.view(np.int16)).to(DEV).view(torch.bfloat16)
     act = torch.empty((T, I), dtype=torch.int16, device=DEV)
     y = torch.full((T, Hout), float("nan"), dtype=torch.float32, device=DEV)
-    nqp.mlp(gu, down, x, act, y, T)
+    if launches == 1:
+        assert nqp.mlp_one_launch_ok(H, I, Hout, T, bits_gu, bits_down)
+    nqp.mlp(gu, down, x, act, y, T, launches=launches or 0)
     assert nqp.last_device_error() == 0
     tol_act, y_ref, e_ref = _check_act(act.cpu().numpy().view(np.uint16), cg, sg, cu, su, xb, cd, sd)
     w_abs = np.abs(oracle.dequant(cd, sd))
     bound = oracle.REL_TOL * e_ref + oracle.ABS_TOL + tol_act @ w_abs.T
     err = np.abs(y.cpu().numpy() - y_ref)
     assert np.all(err <= bound), np.max(err / bound)
+    return gu, down, x, act, y
 
 
 @pytest.mark.parametrize("T", [1, 4, 8])
@@ -123,7 +133,95 @@ def test_mlp_layer_other_widths(bits_gu, bits_down, T):
 
 
 @pytest.mark.slow
-def test_mlp_layer_full_size():
+@pytest.mark.parametrize("bits_down,T", [(5, 1), (4, 2), (5, 8)])
+def test_mlp_layer_full_size(bits_down, T):
     """Qwen3.8-27B-shaped layer: gate+up 5120 -> 2 x 17408 (4-bit), down
-    17408 -> 5120 (5-bit), one token."""
-    _check_layer(I=17408, H=5120, Hout=5120, bits_gu=4, bits_down=5, T=1, tag=(703,))
+    17408 -> 5120 (5-bit for layers 0-35, 4-bit for 36-63), in one launch."""
+    _check_layer(I=17408, H=5120, Hout=5120, bits_gu=4, bits_down=bits_down, T=T,
+                 tag=(703, bits_down, T), launches=1)
+    _check_layer(I=17408, H=5120, Hout=5120, bits_gu=4, bits_down=bits_down, T=T,
+                 tag=(703, bits_down, T), launches=2)
+
+
+@pytest.mark.parametrize("bits_gu,bits_down,T,I", [(4, 5, 1, 8704), (4, 5, 2, 8704), (4, 5, 4, 8704),
+                                                   (4, 5, 8, 8704), (4, 4, 3, 8704), (6, 4, 8, 8704),
+                                                   (8, 8, 2, 8704), (4, 5, 1, 4352), (4, 5, 2, 4352),
+                                                   (4, 4, 2, 4352)])
+def test_mlp_one_launch_matches_two_launches(bits_gu, bits_down, T, I):
+    """The one-launch layer (gate+up phase publishing its activations, the down
+    phase in the same kernel) against the oracle, and bit for bit against the
+    two-launch path (the same products in the same order).  I = 8704: the
+    down product takes a K split of 2; I = 4352: no split, and the gate+up
+    phase has so few tiles per CTA that the down phase's first stages reach
+    the shared-memory area where the gate+up phase staged x in fp16 (T <= 2),
+    which must wait until that x has been taken."""
+    H, Hout = 1024, 600
+    gu, down, x, act, y = _check_layer(I=I, H=H, Hout=Hout, bits_gu=bits_gu, bits_down=bits_down,
+                                       T=T, tag=(705, bits_gu, bits_down, T, I), launches=1)
+    act2 = torch.empty_like(act)
+    y2 = torch.full_like(y, float("nan"))
+    nqp.mlp(gu, down, x, act2, y2, T, launches=2)
+    assert nqp.last_device_error() == 0
+    assert torch.equal(act, act2)
+    assert torch.equal(y.view(torch.int32), y2.view(torch.int32))
+
+
+def test_mlp_one_launch_limits():
+    """The one-launch kernel's limits: T <= 8, gate+up K <= 5120, the
+    instantiated width pairs; outside them nq_mlp_ex(launches=1) is
+    NQ_EUNSUPPORTED and the default (two launches) still runs."""
+    assert nqp.mlp_one_launch_ok(5120, 17408, 5120, 8, 4, 5)
+    assert not nqp.mlp_one_launch_ok(5120, 17408, 5120, 9, 4, 5)
+    assert not nqp.mlp_one_launch_ok(6144, 1024, 512, 1, 4, 5)
+    assert not nqp.mlp_one_launch_ok(1024, 1024, 512, 1, 5, 6)
+    cg, sg, cu, su, xb, packed, sp = _gate_up_case((707,), 5, 1024, 512, 1)
+    gu = nqp.QuantizedWeight(packed, sp, 512, 2048, 5)
+    cd = np.zeros((64, 1024), np.int8)
+    sd = np.zeros((64, 16), np.uint16)
+    pd, spd = _upload(cd, sd, 6)
+    down = nqp.QuantizedWeight(pd, spd, 1024, 64, 6)
+    x = torch.from_numpy(xb.view(np.int16)).to(DEV).view(torch.bfloat16)
+    act = torch.empty((1, 1024), dtype=torch.int16, device=DEV)
+    y = torch.empty((1, 64), dtype=torch.float32, device=DEV)
+    with pytest.raises(nqp.NQError) as e:
+        nqp.mlp(gu, down, x, act, y, 1, launches=1)
+    assert e.value.code == nqp.EUNSUPPORTED
+    nqp.mlp(gu, down, x, act, y, 1)
+    assert nqp.last_device_error() == 0
+    assert np.all(y.cpu().numpy() == 0)
+
+
+def test_mlp_one_launch_repeat_and_graph():
+    """Ten one-launch layers back to back on a stream, then the same ten
+    captured in a CUDA graph and replayed twice: every output equals the
+    first eager result bit for bit (the per-launch activation counters are
+    reset by each launch)."""
+    I, H, Hout, T = 4352, 1024, 600, 2
+    gu, down, x, act, y = _check_layer(I=I, H=H, Hout=Hout, bits_gu=4, bits_down=5, T=T,
+                                       tag=(706,), launches=1)
+    ref_act, ref_y = act.clone(), y.clone()
+    acts = [torch.empty_like(act) for _ in range(10)]
+    ys = [torch.full_like(y, float("nan")) for _ in range(10)]
+    st = torch.cuda.Stream(device=DEV)
+    def run():
+        for a2, y2 in zip(acts, ys):
+            nqp.mlp(gu, down, x, a2, y2, T, launches=1, stream=st)
+    with torch.cuda.stream(st):
+        run()
+    st.synchronize()
+    assert nqp.last_device_error() == 0
+    for a2, y2 in zip(acts, ys):
+        assert torch.equal(a2, ref_act) and torch.equal(y2, ref_y)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        run()
+    for _ in range(2):
+        for y2 in ys:
+            y2.fill_(float("nan"))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(st):
+            g.replay()
+        st.synchronize()
+        assert nqp.last_device_error() == 0
+        for a2, y2 in zip(acts, ys):
+            assert torch.equal(a2, ref_act) and torch.equal(y2, ref_y)

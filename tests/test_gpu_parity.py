@@ -305,6 +305,29 @@ def test_q4_f16_and_bf16_routes_agree(T, monkeypatch):
     monkeypatch.delenv("NQ_X_F16")
 
 
+def test_gemv_right_after_device_pack():
+    """A GEMV launched directly after nq_pack_device on the same stream (no
+    other launch between them) reads the freshly packed weights: the library
+    launches that GEMV without programmatic dependent launch.  x and y are
+    prepared before the packing so that nothing else runs in between."""
+    for bits in (4, 5):
+        case = uniform_case((317, bits), bits, 600, 2048, 3)
+        codes, sb = oracle_inputs(case)
+        dcodes = torch.from_numpy(codes).to(DEV)
+        dsb = torch.from_numpy(sb.view(np.int16)).to(DEV)
+        cb, sbytes = nqp.packed_bytes(case["K"], case["N"], bits)
+        packed = torch.zeros(cb, dtype=torch.uint8, device=DEV)     # stale contents: zeros
+        sp = torch.zeros(sbytes // 2, dtype=torch.int16, device=DEV)
+        x = device_x(torch, case, DEV)
+        y = torch.full((3, case["N"]), float("nan"), dtype=torch.float32, device=DEV)
+        torch.cuda.synchronize()
+        nqp.pack_device(dcodes, dsb, bits, packed=packed, scales_packed=sp)
+        nqp.gemv(packed, sp, x, y, case["K"], case["N"], 3, bits)
+        assert nqp.last_device_error() == 0
+        y_ref, e_ref = oracle.gemv(codes, sb, case["xb"])
+        assert oracle.max_violation(y.cpu().numpy(), y_ref, e_ref) <= 1.0
+
+
 # ---------------------------------------------------------------- errors and edge cases
 def test_invalid_arguments():
     case = rtn_case((311,), 4, 32, 128, 2)
