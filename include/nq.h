@@ -337,6 +337,18 @@ int nq_gemv_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit,
                  int* route_out, int* ksplit_out, int* clusters_out, int* stages_out,
                  int* smem_out);
 
+/* Where the kernel of that plan keeps x (test and benchmark aid). */
+typedef enum {
+  NQ_X_SMEM = 0,     /* a shared-memory x tile, staged once per CTA */
+  NQ_X_REGS = 1,     /* one token block (T <= 8): x fragments in registers */
+  NQ_X_REGS2 = 2,    /* two token blocks (T <= 16), both in registers */
+  NQ_X_HYBRID = 3    /* two token blocks: tokens 0-7 in registers, 8.. in shared memory */
+} nq_x_place;
+
+/* Writes the nq_x_place of the plan nq_gemv_plan reports for the same
+ * arguments to *x_out (host pointer, not null).  Needs a current CUDA device. */
+int nq_gemv_plan_x(int64_t K, int64_t N, int T, int bits, int route, int ksplit, int* x_out);
+
 /* Self-test of the bounded waits: launches one CTA that waits on a barrier
  * nothing will ever complete, with a limit of `limit_us` microseconds; the
  * kernel then gives up, records NQ_ETIMEOUT in the status word and returns.

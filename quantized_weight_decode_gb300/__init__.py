@@ -27,6 +27,8 @@ __all__ = [
 ]
 
 ROUTE_AUTO, ROUTE_MMA, ROUTE_FFMA = 0, 1, 2
+# x placement of a plan (nq_x_place)
+X_PLACES = ("smem", "regs", "regs2", "hybrid")
 OK, EINVAL, EALIGN, ERANGE, ECUDA, ETIMEOUT, EUNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -63,6 +65,7 @@ _SIGS = {
     "nq_dequant": (_i32, [_vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "nq_last_device_error": (_i32, [_vp]),
     "nq_gemv_plan": (_i32, [_i64, _i64, _i32, _i32, _i32, _i32, _ip, _ip, _ip, _ip, _ip]),
+    "nq_gemv_plan_x": (_i32, [_i64, _i64, _i32, _i32, _i32, _i32, _ip]),
     "nq_selftest_wait_timeout": (_i32, [_i32, _vp]),
     "nq_status_string": (ctypes.c_char_p, [_i32]),
     "nq_layout_version": (_i32, []),
@@ -386,7 +389,11 @@ def plan(K: int, N: int, T: int, bits: int, route: int = ROUTE_AUTO, ksplit: int
     _check(lib().nq_gemv_plan(K, N, T, bits, route, ksplit, *[ctypes.byref(v) for v in vals]),
            "nq_gemv_plan")
     keys = ("route", "ksplit", "clusters", "stages", "smem")
-    return {k: v.value for k, v in zip(keys, vals)}
+    out = {k: v.value for k, v in zip(keys, vals)}
+    xp = ctypes.c_int()
+    _check(lib().nq_gemv_plan_x(K, N, T, bits, route, ksplit, ctypes.byref(xp)), "nq_gemv_plan_x")
+    out["x"] = X_PLACES[xp.value]
+    return out
 
 
 def selftest_wait_timeout(limit_us: int, stream=None) -> None:

@@ -71,6 +71,12 @@ constexpr int kXregMaxGroups = 5;  // (the slice-length dispatch covers 1..5)
 // kXreg2MaxGroups groups per warp slice.
 constexpr int kNtokXreg2 = 4;
 constexpr int kXreg2MaxGroups = 3;
+// kNtokXregH: two token blocks (8 < T <= 16) with the first block's x in
+// registers (at most kXregMaxGroups groups per warp slice, as for T <= 8) and
+// the second block's x in shared memory, read per group (two 16-byte loads):
+// twice the groups per warp of kNtokXreg2 for the same registers, so a
+// smaller K split.
+constexpr int kNtokXregH = 5;
 // Row tiles per hand-off: the x-in-register consumers with one token block
 // (T <= 8) take the tiles of their cluster in pairs (two ring stages, two
 // accumulator sets, one partial buffer), which halves the per-job bookkeeping
@@ -225,10 +231,15 @@ __device__ __forceinline__ Work cta_work(const GemvArgs& a) {
   const int ks = a.ksplit;
   const int cl = blockIdx.x / ks;
   w.rank = (ks > 1) ? static_cast<int>(cluster_ctarank()) : 0;
-  const long long nt = a.Nt;
-  w.rt_begin = (static_cast<long long>(cl) * nt) / a.clusters;
-  const long long rt_end = (static_cast<long long>(cl + 1) * nt) / a.clusters;
-  w.njobs = static_cast<int>(rt_end - w.rt_begin);
+  // Contiguous row tiles per cluster; the Nt mod clusters extra tiles go to
+  // the lowest cluster indices.  The grid's CTAs come up in block-index
+  // order over the first 2-4 us, so the first clusters also start first:
+  // on GB300 this ends the launch 1-3 % sooner than spreading the extras
+  // evenly (27B shapes; gate+up 18.55 -> 18.36 us at T = 1, down 13.24 ->
+  // 12.85 us for 4-bit codes at T = 1).
+  const long long nt = a.Nt, base = nt / a.clusters, rem = nt % a.clusters;
+  w.rt_begin = cl * base + min(static_cast<long long>(cl), rem);
+  w.njobs = static_cast<int>(base + (cl < rem ? 1 : 0));
   w.g_begin = (w.rank * a.G) / ks;
   w.g_end = ((w.rank + 1) * a.G) / ks;
   return w;
@@ -906,6 +917,146 @@ __device__ void xreg_jobs(const GemvArgs& a, uint8_t* smem, const Bars& bars, co
   if constexpr (CONT) *pos = RingPos{stage, phase, rb, rn};
 }
 
+// One group of the hybrid kernel: token block 0 against the x fragments in
+// registers (xr), token block 1 against fragments read from the shared x tile
+// (xs: this lane's entry of the group, xh: offset of the second plane; the
+// zero area for lanes whose token is absent).
+template <int BITS>
+__device__ __forceinline__ void mma_group_xrh(const uint8_t* blk, const uint8_t* sc,
+                                              const uint32_t (&xr)[8], const uint8_t* xs, int xh,
+                                              int lane, int q, float (&acc)[2][4]) {
+  uint32_t w[BITS];
+  load_lane_words<BITS>(blk, lane, w);
+  const float2 s = __half22float2(*reinterpret_cast<const __half2*>(sc + 4 * q));
+  const uint4 xa = *reinterpret_cast<const uint4*>(xs);
+  const uint4 xb = *reinterpret_cast<const uint4*>(xs + xh);
+  float d[2][4], dh[2][4];   // dh: high-nibble plane of 8-bit codes
+#pragma unroll
+  for (int js = 0; js < 4; ++js) {
+    uint32_t a0, a1, a2, a3, h0 = 0, h1 = 0, h2 = 0, h3 = 0;
+    if constexpr (BITS == 8) {
+      q8_pair_planes(w, 4 * js + 0, a0, h0);
+      q8_pair_planes(w, 4 * js + 1, a1, h1);
+      q8_pair_planes(w, 4 * js + 2, a2, h2);
+      q8_pair_planes(w, 4 * js + 3, a3, h3);
+    } else {
+      a0 = pair_codes_bf16<BITS>(w, 4 * js + 0);
+      a1 = pair_codes_bf16<BITS>(w, 4 * js + 1);
+      a2 = pair_codes_bf16<BITS>(w, 4 * js + 2);
+      a3 = pair_codes_bf16<BITS>(w, 4 * js + 3);
+    }
+    const uint32_t b0 = js == 0 ? xa.x : js == 1 ? xa.z : js == 2 ? xb.x : xb.z;
+    const uint32_t b1 = js == 0 ? xa.y : js == 1 ? xa.w : js == 2 ? xb.y : xb.w;
+    if (js == 0) {
+      mma_16816_zc(d[0], a0, a1, a2, a3, xr[0], xr[1]);
+      mma_16816_zc(d[1], a0, a1, a2, a3, b0, b1);
+      if constexpr (BITS == 8) {
+        mma_16816_zc(dh[0], h0, h1, h2, h3, xr[0], xr[1]);
+        mma_16816_zc(dh[1], h0, h1, h2, h3, b0, b1);
+      }
+    } else {
+      mma_16816(d[0], a0, a1, a2, a3, xr[2 * js], xr[2 * js + 1]);
+      mma_16816(d[1], a0, a1, a2, a3, b0, b1);
+      if constexpr (BITS == 8) {
+        mma_16816(dh[0], h0, h1, h2, h3, xr[2 * js], xr[2 * js + 1]);
+        mma_16816(dh[1], h0, h1, h2, h3, b0, b1);
+      }
+    }
+  }
+  if constexpr (BITS == 8) {
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) d[nb][e] = fmaf(16.f, dh[nb][e], d[nb][e]);
+  }
+#pragma unroll
+  for (int nb = 0; nb < 2; ++nb) {
+    acc[nb][0] = fmaf(s.x, d[nb][0], acc[nb][0]);
+    acc[nb][1] = fmaf(s.x, d[nb][1], acc[nb][1]);
+    acc[nb][2] = fmaf(s.y, d[nb][2], acc[nb][2]);
+    acc[nb][3] = fmaf(s.y, d[nb][3], acc[nb][3]);
+  }
+}
+
+// The hybrid kernel's job loop for a slice of NG groups (one row tile per
+// hand-off).  xs0: this lane's entry of the slice's first group in the shared
+// x tile; xstep: bytes between groups; xh: the second plane's offset.
+template <int BITS, int NG>
+__device__ void xregh_jobs(const GemvArgs& a, uint8_t* smem, const Bars& bars, const Waiter& wt,
+                           const Work& wk, int warp, int lane, int codes_off, int scales_off,
+                           const uint32_t (&xr)[kXregMaxGroups][1][8], const uint8_t* xs0,
+                           int xstep, int xh) {
+  const int q = lane >> 2;
+  const uint8_t* ring = smem + a.off_ring;
+  int stage = 0;
+  uint32_t phase = 0;
+  int rb = 0;
+  uint32_t rn = 0;
+  for (int j = 0; j < wk.njobs; ++j) {
+    float acc[2][4];
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
+    if (!wt.wait_warp<false>(bars.full(stage), phase)) return;
+    const uint8_t* st = ring + stage * a.stage_bytes;
+#pragma unroll
+    for (int i = 0; i < NG; ++i)
+      mma_group_xrh<BITS>(st + codes_off + i * (128 * BITS), st + scales_off + i * kScaleBytesPerBlock,
+                          xr[i][0], xs0 + i * xstep, xh, lane, q, acc);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars.empty(stage));
+    if (++stage == a.stages) { stage = 0; phase ^= 1; }
+    if (!hand_partial_mma<2>(a, smem, bars, wt, warp, lane, rb, rn, acc)) return;
+    if (++rb == a.nbuf) { rb = 0; ++rn; }
+  }
+}
+
+// Hybrid consumer: token block 0's x fragments of the warp's fixed slice in
+// registers, token block 1's (tokens 8 ..) in the shared x tile, which the
+// consumer warps stage once in B-fragment order (stage_x_bf16's layout over
+// tokens 8 .. T-1, as if x started at token 8).
+template <int BITS>
+__device__ void consumer_xregh(const GemvArgs& a, uint8_t* smem, const Bars& bars,
+                               const Waiter& wt, const Work& wk, int warp, int lane) {
+  constexpr int kBlock = 128 * BITS;
+  const Slice sl = warp_slice(wk, warp);
+  const int n = sl.ge - sl.gs;  // <= kXregMaxGroups
+  const int rel = sl.gs - wk.g_begin;
+  const int codes_off = rel * kBlock;
+  const int scales_off = a.stage_groups * kBlock + rel * kScaleBytesPerBlock;
+  uint32_t xr[kXregMaxGroups][1][8];
+  load_x_frags<kXregMaxGroups, 1>(a, sl, n, lane, xr);
+  // Stage tokens 8 .. T-1 (T2 = T - 8 of them).
+  GemvArgs b2 = a;
+  b2.x = a.x + 8LL * a.K;
+  b2.T = a.T - 8;
+  stage_x_bf16(b2, smem, wk, threadIdx.x, kWarps * 32);
+  asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+  const int q = lane >> 2;
+  const int T2 = a.T - 8;
+  const bool v = q < T2;
+  const uint8_t* xs0 = v ? smem + a.off_x + ((rel * T2 + q) * 4 + (lane & 3)) * 16
+                         : smem + kZeroAreaOffset;
+  const int xstep = v ? T2 * 64 : 0;
+  const int xh = v ? (wk.g_end - wk.g_begin) * T2 * 64 : 16;  // the zero area holds 32 bytes
+#define NQ_XREGH_CASE(k)                                                                   \
+  case k:                                                                                  \
+    xregh_jobs<BITS, k>(a, smem, bars, wt, wk, warp, lane, codes_off, scales_off, xr, xs0, \
+                        xstep, xh);                                                        \
+    break;
+  switch (n) {
+    NQ_XREGH_CASE(1)
+    NQ_XREGH_CASE(2)
+    NQ_XREGH_CASE(3)
+    NQ_XREGH_CASE(4)
+    NQ_XREGH_CASE(5)
+    default:
+      xregh_jobs<BITS, 0>(a, smem, bars, wt, wk, warp, lane, codes_off, scales_off, xr, xs0,
+                          xstep, xh);
+      break;
+  }
+#undef NQ_XREGH_CASE
+}
+
 // The slice length n (uniform per warp, <= GWM) picks the job loop once.
 template <int BITS, int GWM, int NT, bool F16, bool CONT = false>
 __device__ __forceinline__ void run_xreg_jobs(const GemvArgs& a, uint8_t* smem, const Bars& bars,
@@ -1545,7 +1696,8 @@ __global__ void __launch_bounds__(kThreads, 1) nq_gemv_kernel(const __grid_const
     // Value slots per lane: 16 x T values over 32 lanes.
     // Value slots per lane: JT x 16 x T values over 32 lanes, four each.
     constexpr int JT = kJobTiles<ROUTE, NTOK>;
-    constexpr int kTokBlocks = (ROUTE == kRouteMma && (NTOK == 2 || NTOK == kNtokXreg2)) ? 2 : 1;
+    constexpr int kTokBlocks =
+        (ROUTE == kRouteMma && (NTOK == 2 || NTOK == kNtokXreg2 || NTOK == kNtokXregH)) ? 2 : 1;
     epilogue<JT * kTokBlocks, JT>(a, smem, bars, wt, wk, ew, lane);
   } else {
     griddep_wait();
@@ -1553,6 +1705,8 @@ __global__ void __launch_bounds__(kThreads, 1) nq_gemv_kernel(const __grid_const
       consumer_xreg<BITS, kXregMaxGroups, 1>(a, smem, bars, wt, wk, warp, lane);
     } else if constexpr (ROUTE == kRouteMma && NTOK == kNtokXreg2) {
       consumer_xreg<BITS, kXreg2MaxGroups, 2>(a, smem, bars, wt, wk, warp, lane);
+    } else if constexpr (ROUTE == kRouteMma && NTOK == kNtokXregH) {
+      consumer_xregh<BITS>(a, smem, bars, wt, wk, warp, lane);
     } else {
       if constexpr (ROUTE == kRouteMma) {
         stage_x_bf16(a, smem, wk, threadIdx.x, kWarps * 32);

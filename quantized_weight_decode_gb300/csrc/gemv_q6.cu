@@ -7,6 +7,7 @@ const void* gemv_kernel_q6(int route, int ntok) {
   if (route == kRouteMma) {
     if (ntok == kNtokXreg) return reinterpret_cast<const void*>(&nq_gemv_kernel<6, kRouteMma, kNtokXreg>);
     if (ntok == kNtokXreg2) return reinterpret_cast<const void*>(&nq_gemv_kernel<6, kRouteMma, kNtokXreg2>);
+    if (ntok == kNtokXregH) return reinterpret_cast<const void*>(&nq_gemv_kernel<6, kRouteMma, kNtokXregH>);
     return ntok == 1 ? reinterpret_cast<const void*>(&nq_gemv_kernel<6, kRouteMma, 1>)
                      : reinterpret_cast<const void*>(&nq_gemv_kernel<6, kRouteMma, 2>);
   }

@@ -166,9 +166,13 @@ bool layout_nbuf(const Plan& base, int G, int T, int bits, int ks, int sg, int m
   p.sg = sg;
   p.nbuf = nbuf;
   const int gc_max = (G + ks - 1) / ks;
-  const bool x_in_regs = p.route == NQ_ROUTE_MMA && (p.ntok == kNtokXreg || p.ntok == kNtokXreg2);
+  const bool x_in_regs = p.route == NQ_ROUTE_MMA &&
+                         (p.ntok == kNtokXreg || p.ntok == kNtokXreg2 || p.ntok == kNtokXregH);
+  // The hybrid kernel keeps the second token block's x in shared memory.
   const long long x_bytes =
-      x_in_regs ? 0 : 1LL * gc_max * T * (p.route == NQ_ROUTE_MMA ? 128 : 256);
+      p.ntok == kNtokXregH ? 1LL * gc_max * (T - 8) * 128
+      : x_in_regs          ? 0
+                           : 1LL * gc_max * T * (p.route == NQ_ROUTE_MMA ? 128 : 256);
   const int jt = (x_in_regs && p.ntok == kNtokXreg) ? 2 : 1;   // the kernel's kJobTiles
   const int red_bytes = p.nbuf * kWarps * jt * 16 * T * 4;
   const int cl_bytes = ks > 1 ? p.nbuf * (ks - 1) * jt * 16 * T * 4 : 0;
@@ -216,8 +220,9 @@ bool layout_nbuf(const Plan& base, int G, int T, int bits, int ks, int sg, int m
 // kEpiWarps: each buffer belongs to one epilogue warp.
 bool layout_for(const Plan& base, int G, int T, int bits, int ks, int sg, int min_stages,
                 int smem_optin, int extra, Plan* out) {
-  const bool x_in_regs =
-      base.route == NQ_ROUTE_MMA && (base.ntok == kNtokXreg || base.ntok == kNtokXreg2);
+  const bool x_in_regs = base.route == NQ_ROUTE_MMA && (base.ntok == kNtokXreg ||
+                                                        base.ntok == kNtokXreg2 ||
+                                                        base.ntok == kNtokXregH);
   const int jt = (x_in_regs && base.ntok == kNtokXreg) ? 2 : 1;
   int std_nbuf, deep_nbuf;
   if (jt == 2) {
@@ -340,14 +345,31 @@ int make_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, Plan
   base.ntok = route == NQ_ROUTE_MMA ? (T <= 8 ? 1 : 2) : kFfmaMaxT;
   base.func = kernel_for(bits, route, base.ntok);
   if (int rc = prepare_func(dev, base.func, d->smem_optin)) return rc;
-  // x-in-register variant: one token block (T <= 8, slices of up to
-  // kXregMaxGroups groups) or two (T <= 16, up to kXreg2MaxGroups).
-  Plan xreg = base;
-  xreg.ntok = T <= 8 ? kNtokXreg : kNtokXreg2;
-  xreg.func = kernel_for(bits, route, xreg.ntok);
-  const int xreg_max_groups = T <= 8 ? kXregMaxGroups : kXreg2MaxGroups;
+  // x-in-register variants, in order of preference at one K split: one
+  // token block (T <= 8, warp slices of up to kXregMaxGroups groups); for two
+  // blocks (T <= 16) both in registers (up to kXreg2MaxGroups), else the
+  // hybrid with the second block in shared memory (up to kXregMaxGroups).
+  // NQ_XREGH=0 leaves the hybrid out, NQ_XREGH=1 takes only the hybrid.
+  struct XregVariant {
+    Plan plan;
+    int max_groups;
+  };
+  XregVariant xv[2];
+  int nxv = 0;
   if (route == NQ_ROUTE_MMA) {
-    if (int rc = prepare_func(dev, xreg.func, d->smem_optin)) return rc;
+    const int hyb = env_int("NQ_XREGH", -1);
+    const int ntoks[2] = {T <= 8 ? kNtokXreg : (hyb == 1 ? 0 : kNtokXreg2),
+                          T <= 8 || hyb == 0 ? 0 : kNtokXregH};
+    for (int ntok : ntoks) {
+      if (ntok == 0) continue;
+      Plan xr = base;
+      xr.ntok = ntok;
+      xr.func = kernel_for(bits, route, ntok);
+      if (int rc = prepare_func(dev, xr.func, d->smem_optin)) return rc;
+      xv[nxv].plan = xr;
+      xv[nxv].max_groups = ntok == kNtokXreg2 ? kXreg2MaxGroups : kXregMaxGroups;
+      ++nxv;
+    }
   }
 
   const int G = static_cast<int>(K / kGroup);
@@ -361,8 +383,12 @@ int make_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, Plan
   // in shared memory; T = 12 and 16, K = 5120: KS 2, 205 / 213 us on the
   // 248,320-row head against 230 / 372 us at KS 1 with x in shared memory) --
   // because its consumers issue the fewest instructions per weight, and the
-  // split's per-job overhead grows with KS.  No such candidate: the time
-  // model below decides.
+  // split's per-job overhead grows with KS.  For T > 8 the hybrid's smaller
+  // split pays (gate+up T = 16: KS 1, 27.3 us against 29.0 us with both
+  // blocks in registers at KS 2; 5-bit down T = 16: KS 4, 19.1 us against
+  // 24.1 us; head T = 12: KS 1, 170.7 against 194.6 us), but at an equal
+  // split both blocks in registers are faster (head T = 16, KS 2: 197.0
+  // against 203.8 us).  No such candidate: the time model below decides.
   bool have_xreg = false;
   Plan best_xreg;
   for (int ks : cands) {
@@ -372,10 +398,12 @@ int make_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, Plan
     const int gw_max = (gc_max + kWarps - 1) / kWarps;
     Plan p;
     bool fit = false;
-    if (route == NQ_ROUTE_MMA && gw_max <= xreg_max_groups) {
+    for (int v = 0; v < nxv && !fit; ++v) {
       // x held in registers; a stage is the CTA's whole K range of one job.
-      fit = layout_for(xreg, G, T, bits, ks, gc_max, 2, d->smem_optin, extra, &p);
+      if (gw_max <= xv[v].max_groups)
+        fit = layout_for(xv[v].plan, G, T, bits, ks, gc_max, 2, d->smem_optin, extra, &p);
     }
+    const bool is_xreg = fit;
     // Otherwise x in shared memory; a stage is the job's K range cut into
     // `parts` equal pieces, the fewest that leave at least 3 stages (2 when
     // a piece is down to one group per warp).
@@ -393,7 +421,7 @@ int make_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, Plan
       best = p;
       have = true;
     }
-    if (!have_xreg && route == NQ_ROUTE_MMA && ks <= 4 && p.func == xreg.func) {
+    if (!have_xreg && ks <= 4 && is_xreg) {
       best_xreg = p;
       have_xreg = true;
     }
@@ -1102,6 +1130,18 @@ int nq_gemv_plan(int64_t K, int64_t N, int T, int bits, int route, int ksplit, i
   if (clusters_out) *clusters_out = p.clusters;
   if (stages_out) *stages_out = p.stages;
   if (smem_out) *smem_out = p.smem;
+  return NQ_OK;
+}
+
+int nq_gemv_plan_x(int64_t K, int64_t N, int T, int bits, int route, int ksplit, int* x_out) {
+  if (!x_out) return NQ_EINVAL;
+  Plan p;
+  if (int rc = make_plan(K, N, T, bits, route, ksplit, &p)) return rc;
+  *x_out = p.route != NQ_ROUTE_MMA ? NQ_X_SMEM
+           : p.ntok == kNtokXreg   ? NQ_X_REGS
+           : p.ntok == kNtokXreg2  ? NQ_X_REGS2
+           : p.ntok == kNtokXregH  ? NQ_X_HYBRID
+                                   : NQ_X_SMEM;
   return NQ_OK;
 }
 

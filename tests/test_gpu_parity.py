@@ -156,6 +156,66 @@ def test_many_jobs_per_cluster():
         _check(case, _y(case, packed, sp, route=nqp.ROUTE_MMA, ksplit=ks))
 
 
+# ---------------------------------------------------------------- two token blocks, hybrid x
+# (K, N, K split): whole warp slices of 5 groups, uneven slices, K splits 2 and 4
+HYBRID_SHAPES = [(2560, 300, 1), (1088, 37, 1), (4096, 170, 2), (8192, 50, 4)]
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
+@pytest.mark.parametrize("T", [9, 11, 16])
+def test_hybrid_x_parity(bits, T, monkeypatch):
+    """T > 8 through the kernel that keeps tokens 0-7 in registers and tokens
+    8.. in shared memory: ragged row tiles, uneven warp slices, K splits 1 to
+    4, element by element against the oracle."""
+    monkeypatch.setenv("NQ_XREGH", "1")
+    # five groups per warp at K = 5120: the x tile (T - 8) x 10 KB and two
+    # stages fit next to each other up to 5-bit codes at every T
+    shapes = HYBRID_SHAPES + ([(5120, 200, 1)] if bits <= 5 else [])
+    for i, (K, N, ks) in enumerate(shapes):
+        assert nqp.plan(K, N, T, bits, route=nqp.ROUTE_MMA, ksplit=ks)["x"] == "hybrid"
+        case = uniform_case((330, bits, T, i), bits, N, K, T) if i % 2 else \
+            rtn_case((330, bits, T, i), bits, N, K, T)
+        packed, sp = device_weight(nqp, torch, case, DEV)
+        _check(case, _y(case, packed, sp, route=nqp.ROUTE_MMA, ksplit=ks))
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_hybrid_x_one_hot_tokens_exact(bits, monkeypatch):
+    """One-hot x at T = 12 (tokens 8-11 come from the shared-memory tile):
+    every token's output is its weight column exactly, for both two-block
+    kernels."""
+    case = uniform_case((331, bits), bits, 90, 2560, 12)
+    codes, sb = oracle_inputs(case)
+    packed, sp = _upload_packed(codes, sb, bits)
+    ks_cols = [0, 63, 64, 511, 512, 1000, 1279, 1280, 2047, 2100, 2558, 2559]
+    xb = np.zeros((12, 2560), np.uint16)
+    for t, k in enumerate(ks_cols):
+        xb[t, k] = 0x3F80
+    c2 = dict(case, xb=xb)
+    wref = oracle.dequant_f32(codes, sb)
+    for env, place in (("1", "hybrid"), ("0", "regs2")):
+        monkeypatch.setenv("NQ_XREGH", env)
+        for ks in (1, 2):
+            pl = nqp.plan(2560, 90, 12, bits, route=nqp.ROUTE_MMA, ksplit=ks)
+            assert pl["x"] == place, (env, ks, pl)
+            y = _y(c2, packed, sp, route=nqp.ROUTE_MMA, ksplit=ks)
+            for t in range(12):
+                assert np.array_equal(y[t], wref[:, ks_cols[t]]), (env, ks, t)
+
+
+def test_two_block_kernel_choice():
+    """The planner's measured rule for T > 8: the hybrid where it allows a
+    smaller K split than both blocks in registers, both in registers at an
+    equal split."""
+    p = nqp.plan(5120, 34816, 16, 4)      # gate+up: hybrid at KS 1 (regs2 needs KS 2)
+    assert (p["x"], p["ksplit"]) == ("hybrid", 1), p
+    p = nqp.plan(17408, 5120, 12, 5)      # down: hybrid at KS 4 (regs2 needs KS 8)
+    assert (p["x"], p["ksplit"]) == ("hybrid", 4), p
+    p = nqp.plan(5120, 248320, 16, 6)     # head: the hybrid does not fit at KS 1
+    assert (p["x"], p["ksplit"]) == ("regs2", 2), p
+    assert nqp.plan(5120, 34816, 8, 4)["x"] == "regs"
+
+
 # ---------------------------------------------------------------- exact invariants
 def _upload_packed(codes, sb, bits):
     hp, hs = nqp.pack(codes, sb, bits)
