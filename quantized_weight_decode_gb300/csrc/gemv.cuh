@@ -111,8 +111,9 @@ struct GemvArgs {
   // Fused verify head (h_ws != nullptr): per token t the argmax, the maximum
   // and the logsumexp of y[t, 0..N), reduced through the workspace h_ws
   // (layout: kHeadCounterBytes of arrival counters -- [0] all groups, [1 + g]
-  // group g -- then one kHeadStateBytes state per (cluster, epilogue warp,
-  // token), then one per (group of kHeadGroup clusters, token)).  y may then
+  // group g -- then one kHeadStateBytes state per (unit, epilogue warp,
+  // token), then one per (group of kHeadGroup units, token); a unit is a
+  // cluster, or a CTA where the K split finalises by reduce-scatter).  y may then
   // be null (logits not stored).
   uint8_t* h_ws;
   int* h_argmax;
@@ -124,7 +125,7 @@ struct GemvArgs {
   // ([T, N / 2] bf16 bits, N a multiple of 16).
   uint16_t* act;
   // Top-k of the fused head (tk_k > 0, 1 <= tk_k <= kTopkMax): epilogue
-  // warp w of cluster c keeps, per token t, the 32 largest keys of the logits
+  // warp w of unit c keeps, per token t, the 32 largest keys of the logits
   // it finalised in tk_lists[((c * kEpiWarps + w) * kHeadMaxT + t) * 32 ...]
   // (sorted descending; what the merge kernel reads), its candidate buffer in
   // tk_bufs (64 keys per list, same indexing), and the buffer counts in
@@ -161,8 +162,8 @@ constexpr int kSyncSlots = kSyncSlotsEager + kSyncSlotsCapture;
 constexpr int kHeadCounterBytes = 256;
 constexpr int kHeadStateBytes = 16;
 constexpr int kHeadMaxT = 16;
-constexpr int kHeadGroup = 8;       // clusters merged per group (first level)
-constexpr int kHeadMaxGroups = 32;  // groups the second level covers (256 clusters)
+constexpr int kHeadGroup = 8;       // units (clusters or CTAs) merged per group (first level)
+constexpr int kHeadMaxGroups = 32;  // groups the second level covers (256 units)
 
 // Shared-memory map of the barrier region (first 1 KiB).
 struct Bars {
@@ -1294,6 +1295,29 @@ __device__ __forceinline__ void head_push(float& m, float& s, int& a, float v, i
     s += __expf(v - m);
   }
 }
+// The same after the four logits of rows idx0 .. idx0 + 3: the batch's
+// maximum first (one rescale at most), then one term per logit without
+// branches.  Rows arrive in increasing order, so on equal maxima the state's
+// index is the smaller one.
+__device__ __forceinline__ void head_push4(float& m, float& s, int& a, const float4& v, int idx0) {
+  const float x[4] = {v.x, v.y, v.z, v.w};
+  float mb = -INFINITY;  // (NaN never becomes the maximum)
+  int ib = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    if (x[c] > mb) {
+      mb = x[c];
+      ib = c;
+    }
+  if (mb > m) {
+    s *= __expf(m - mb);  // 0 for the empty state (m = -inf, s = 0)
+    m = mb;
+    a = idx0 + ib;
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    s += x[c] == -INFINITY ? 0.f : x[c] == m ? 1.f : __expf(x[c] - m);
+}
 __device__ __forceinline__ void head_merge(float& m, float& s, int& a, float mo, float so, int ao) {
   if (mo == -INFINITY && so == 0.f) return;
   if (m == -INFINITY && s == 0.f) {
@@ -1419,6 +1443,86 @@ __device__ void head_finish(const GemvArgs& a, const Work& wk, int ew, int lane,
   }
 }
 
+// head_finish for epilogue_rs: every CTA publishes states (the ranks of a
+// cluster finalise different slots), so the merge runs over CTAs.
+template <int SLOTS>
+__device__ void head_finish_cta(const GemvArgs& a, const Work& wk, int ew, int lane,
+                            const float (&hm)[SLOTS], const float (&hs)[SLOTS],
+                            const int (&ha)[SLOTS], const int (&vtok)[SLOTS]) {
+  const int T = a.T;
+  const int units = a.clusters * a.ksplit;  // CTAs publishing states
+  const int cl = static_cast<int>(blockIdx.x);
+  const int grp = cl / kHeadGroup;
+  const int ngroups = (units + kHeadGroup - 1) / kHeadGroup;
+  const int gcl0 = grp * kHeadGroup;                              // first unit of the group
+  const int gcls = min(kHeadGroup, units - gcl0);                // units in the group
+  unsigned* counters = reinterpret_cast<unsigned*>(a.h_ws);
+  uint8_t* states = a.h_ws + kHeadCounterBytes;                  // (unit, warp, token)
+  uint8_t* gstates = states + static_cast<size_t>(units) * kEpiWarps * kHeadMaxT * kHeadStateBytes;
+  for (int t = 0; t < T; ++t) {
+    float m = -INFINITY, s = 0.f;
+    int am = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < SLOTS; ++i)
+      if (vtok[i] == t) head_merge(m, s, am, hm[i], hs[i], ha[i]);
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) head_merge_lanes(m, s, am, d);
+    if (lane == 0) {
+      const int me = cl * kEpiWarps + ew;
+      *reinterpret_cast<float4*>(states + (static_cast<size_t>(me) * kHeadMaxT + t) * kHeadStateBytes) =
+          make_float4(m, s, __int_as_float(am), 0.f);
+    }
+  }
+  __threadfence();
+  __syncwarp();
+  unsigned last = 0;
+  if (lane == 0)
+    last = atomicAdd(counters + 1 + grp, 1u) == static_cast<unsigned>(gcls * kEpiWarps - 1);
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  __threadfence();
+  // First level: this group's states.
+  const int tok = lane >> 1, half = lane & 1;
+  {
+    constexpr int kHalf = kHeadGroup * kEpiWarps / 2;
+    float m = -INFINITY, s = 0.f;
+    int am = INT_MAX;
+    if (tok < T) {
+      const int n = gcls * kEpiWarps;
+      const int first = half * kHalf;
+      head_merge_entries<kHalf>(states, gcl0 * kEpiWarps + first, max(0, min(kHalf, n - first)),
+                                tok, m, s, am);
+    }
+    head_merge_lanes(m, s, am, 1);
+    if (half == 0 && tok < T)
+      *reinterpret_cast<float4*>(gstates + (static_cast<size_t>(grp) * kHeadMaxT + tok) * kHeadStateBytes) =
+          make_float4(m, s, __int_as_float(am), 0.f);
+    if (lane == 0) *reinterpret_cast<volatile unsigned*>(counters + 1 + grp) = 0u;
+  }
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) last = atomicAdd(counters, 1u) == static_cast<unsigned>(ngroups - 1);
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  __threadfence();
+  // Second level: every group, in order.
+  {
+    constexpr int kHalf = kHeadMaxGroups / 2;
+    float m = -INFINITY, s = 0.f;
+    int am = INT_MAX;
+    if (tok < T) {
+      const int first = half * kHalf;
+      head_merge_entries<kHalf>(gstates, first, max(0, min(kHalf, ngroups - first)), tok, m, s,
+                                am);
+    }
+    head_merge_lanes(m, s, am, 1);
+    if (half == 0 && tok < T) {
+      a.h_argmax[tok] = am == INT_MAX ? -1 : am;
+      a.h_max[tok] = m;
+      a.h_lse[tok] = m + __logf(s);
+    }
+    if (lane == 0) *reinterpret_cast<volatile unsigned*>(counters) = 0u;
+  }
+}
+
 // Shared-memory bytes of the top-k buffer counts (all epilogue warps).
 constexpr int kTopkSmemBytes = kEpiWarps * kHeadMaxT * 4;
 
@@ -1474,6 +1578,332 @@ __device__ __forceinline__ void topk_update(const GemvArgs& a, unsigned long lon
     full &= full - 1;
     topk_flush(list, buf, cnt, t, lane);
   }
+}
+
+// topk_flush and topk_update for epilogue_rs (which keeps each slot's
+// threshold in registers).  Folds the candidate buffer of token t into its list: at
+// most two rounds of sort 32 + merge.  Whole warp; list and buf are this
+// warp's own (global memory, written and read by this warp only).  Returns,
+// in every lane, the list's new k-th key.
+__device__ __forceinline__ unsigned long long topk_flush_kth(unsigned long long* list,
+                                                         unsigned long long* buf, int* cnt, int t,
+                                                         int lane, int k) {
+  const int n = cnt[t];
+  unsigned long long* lt = list + t * 32;
+  unsigned long long m = lt[lane];
+  for (int base = 0; base < n; base += 32) {
+    unsigned long long c = base + lane < n ? buf[t * 64 + base + lane] : 0ull;
+    c = warp_sort_desc(c, lane);
+    m = warp_top32_of_two(m, c, lane);
+  }
+  __syncwarp();
+  lt[lane] = m;
+  if (lane == 0) cnt[t] = 0;
+  __syncwarp();
+  return __shfl_sync(0xffffffffu, m, k - 1);
+}
+
+// One hand-off's logits into the warp's top-k state (the selection scheme of
+// warp-level k-selection: cheap filtering against a threshold, sorting only
+// in batches).  A logit whose key beats the k-th key of its token's list
+// (a lower bound of the warp's k-th largest so far) is appended to the
+// token's buffer; a buffer holding 32 or more keys after the hand-off is
+// folded into the list.  A hand-off adds at most JT x 16 <= 32 keys per
+// token, so a buffer (64 keys) never overflows.  ok[i]: slot i holds logits
+// (rows rbase[i] .. rbase[i] + 3, those below N) of token vtok[i]; thr[i]:
+// the k-th key of that token's list, kept in registers (a lane's slots keep
+// their tokens) and refreshed when the list changes.
+template <int SLOTS>
+__device__ __forceinline__ void topk_update_thr(const GemvArgs& a, unsigned long long* list,
+                                            unsigned long long* buf, int* cnt, int lane,
+                                            const float4 (&v)[SLOTS], const bool (&ok)[SLOTS],
+                                            const long long (&rbase)[SLOTS],
+                                            const int (&vtok)[SLOTS],
+                                            unsigned long long (&thr)[SLOTS]) {
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i) {
+    if (!ok[i]) continue;
+    const int t = vtok[i];
+    const float vv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const unsigned long long key = topk_key(vv[c], static_cast<uint32_t>(rbase[i] + c));
+      if (rbase[i] + c < a.N && key > thr[i]) buf[t * 64 + atomicAdd(cnt + t, 1)] = key;
+    }
+  }
+  __syncwarp();
+  unsigned full = __ballot_sync(0xffffffffu, lane < a.T && cnt[lane] >= 32);
+  while (full) {
+    const int t = __ffs(full) - 1;
+    full &= full - 1;
+    const unsigned long long kth = topk_flush_kth(list, buf, cnt, t, lane, a.tk_k);
+#pragma unroll
+    for (int i = 0; i < SLOTS; ++i)
+      if (vtok[i] == t) thr[i] = kth;
+  }
+}
+
+// K-split exchange as a reduce-scatter (the fused head with two token blocks
+// in registers): slot i of a hand-off (values 128 i .. 128 i + 127, those
+// below nv) is finalised by rank i mod ks; every other rank sends its
+// partials of that slot to that rank.  With one slot in use everything stays
+// on rank 0.  Halves the per-logit softmax work of rank 0 at T = 16 (the
+// fused head 266 -> 252 us, with top-8 385 -> 349 us on GB300); the plain
+// products keep the gather to rank 0, which measured faster for them.
+__device__ __forceinline__ int slot_values(int nv, int i) { return max(0, min(128, nv - 128 * i)); }
+template <int SLOTS>
+__device__ __forceinline__ unsigned slot_owners(int ks, int nv) {
+  unsigned m = 0u;
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i)
+    if (slot_values(nv, i) > 0) m |= 1u << (i % ks);
+  return m;
+}
+
+// Arrivals that complete one use of a rank's exchange-release barrier: one
+// from every other rank that finalises slots (at least 1; unused then).
+template <int SLOTS>
+__device__ __forceinline__ unsigned cl_empty_count(int ks, int nv, int rank) {
+  return max(1, __popc(slot_owners<SLOTS>(ks, nv) & ~(1u << rank)));
+}
+
+// CONT: a phase of the one-launch layer; its hand-offs continue the CTA's
+// sequence after `h0` hand-offs of the previous phase (hand-off g uses
+// buffer g % nbuf and belongs to epilogue warp g % kEpiWarps).
+// The epilogue of the fused head whose K split finalises by reduce-scatter
+// (two token blocks in registers; see slot_owners).  Besides the exchange it
+// differs from epilogue() in the softmax update (head_push4) and in keeping
+// the top-k thresholds in registers; a separate function, so that the
+// other kernels' code stays as it is.
+template <int SLOTS, int JT>
+__device__ inline void epilogue_rs(const GemvArgs& a, uint8_t* smem, const Bars& bars,
+                                   const Waiter& wt, const Work& wk, int ew, int lane) {
+  constexpr bool CONT = false, RS = true;
+  const int h0 = 0;
+  const int T = a.T;
+  const int nvt = 16 * T;            // values per row tile (a multiple of 16)
+  const int nv = JT * nvt;           // values per hand-off (JT consecutive tiles)
+  const int ks = a.ksplit;
+  const float* red = reinterpret_cast<const float*>(smem + a.off_red);
+  float* cl = reinterpret_cast<float*>(smem + a.off_cl);
+  const uint32_t cl_bytes = static_cast<uint32_t>((ks - 1) * nv * 4);
+  // Reduce-scatter (RS, ks > 1): mine[i] = this rank finalises slot i;
+  // in_bytes = what its peers send it per hand-off.
+  bool mine[SLOTS];
+  uint32_t in_bytes = 0;
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i) {
+    mine[i] = !RS || ks == 1 || i % ks == wk.rank;
+    if (RS && ks > 1 && mine[i]) in_bytes += static_cast<uint32_t>((ks - 1) * slot_values(nv, i) * 4);
+  }
+  const bool sends = RS && ks > 1 && (slot_owners<SLOTS>(ks, nv) & ~(1u << wk.rank)) != 0u;
+  auto has = [&](int i) { return 4 * lane + 128 * i < nv; };
+  const bool head = a.h_ws != nullptr;
+  float hm[SLOTS], hs[SLOTS];
+  int ha[SLOTS];
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i) {
+    hm[i] = -INFINITY;
+    hs[i] = 0.f;
+    ha[i] = INT_MAX;
+  }
+  // Tile, token and row of this lane's four values in slot i (fixed per lane).
+  int vt[SLOTS], vtok[SLOTS], vrow[SLOTS];
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i) {
+    const int e = 4 * lane + 128 * i;
+    vt[i] = e / nvt;
+    const int rest = e - vt[i] * nvt;
+    vtok[i] = rest >> 4;
+    vrow[i] = rest & 15;
+  }
+  const int njt = (wk.njobs + JT - 1) / JT;  // hand-offs of this CTA
+  const bool topk = head && a.tk_k > 0 && (RS || ks == 1 || wk.rank == 0);
+  unsigned long long* tk_list = nullptr;
+  unsigned long long* tk_buf = nullptr;
+  int* tk_cnt = nullptr;
+  unsigned long long tk_thr[SLOTS];  // k-th key of each slot's token list (empty: key 0)
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i) tk_thr[i] = 0ull;
+  if (topk) {
+    // one list per CTA (RS: the ranks finalise different rows), else per cluster
+    const size_t me = static_cast<size_t>(RS ? blockIdx.x : blockIdx.x / ks) * kEpiWarps + ew;
+    tk_list = a.tk_lists + me * kHeadMaxT * 32;
+    tk_buf = a.tk_bufs + me * kHeadMaxT * 64;
+    tk_cnt = reinterpret_cast<int*>(smem + a.off_tk) + ew * kHeadMaxT;
+    for (int t = 0; t < T; ++t) tk_list[t * 32 + lane] = 0ull;  // empty keys
+    if (lane < T) tk_cnt[lane] = 0;
+    __syncwarp();
+  }
+  int b = ew;        // buffer of hand-off j (j % nbuf)
+  uint32_t n = 0;    // uses of that buffer so far (j / nbuf)
+  int j = ew;
+  if constexpr (CONT) {
+    j = (ew - h0 % kEpiWarps + kEpiWarps) % kEpiWarps;  // first local hand-off of this warp
+    b = (h0 + j) % a.nbuf;
+    n = static_cast<uint32_t>((h0 + j) / a.nbuf);
+  }
+  for (; j < njt; j += kEpiWarps) {
+    // Cluster-exchange buffer of this hand-off: its position among this
+    // launch's K-split hand-offs, the same on every rank (a continuing phase
+    // starts its own count; its red buffers continue the CTA's count).
+    const int cb = CONT ? j % a.nbuf : b;
+    const uint32_t cn = CONT ? static_cast<uint32_t>(j / a.nbuf) : n;
+    if constexpr (RS) {
+      if (in_bytes != 0u && lane == 0) mbar_arrive_expect_tx_relaxed(bars.cl_full(cb), in_bytes);
+    } else {
+      if (ks > 1 && wk.rank == 0 && lane == 0)
+        mbar_arrive_expect_tx_relaxed(bars.cl_full(cb), cl_bytes);
+    }
+    if (!wt.wait_warp<false>(bars.red_full(b), n & 1u)) return;
+    float4 v[SLOTS];
+#pragma unroll
+    for (int i = 0; i < SLOTS; ++i) {
+      v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (has(i)) {
+        const float* p = red + b * kWarps * nv + 4 * lane + 128 * i;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) add4(v[i], *reinterpret_cast<const float4*>(p + w * nv));
+      }
+    }
+    // Every lane has consumed its loads of the slot (the sums above); a
+    // release here would also wait for the previous job's y stores.
+    mbar_arrive_relaxed(bars.red_empty(b));  // every lane: count 32
+    bool store = true;
+    if constexpr (RS) {
+    if (sends) {
+      // Partials of the slots other ranks finalise: peer r of slot i's owner
+      // o writes area r - (r > o) of o's exchange buffer.
+      if (!wt.wait_warp<false>(bars.cl_empty(cb), (cn & 1u) ^ 1u)) return;
+#pragma unroll
+      for (int i = 0; i < SLOTS; ++i) {
+        if (mine[i] || !has(i)) continue;
+        const int o = i % ks;
+        const int area = wk.rank - (wk.rank > o ? 1 : 0);
+        st_async_v4(map_to_rank(smem_addr(cl + (cb * (ks - 1) + area) * nv + 4 * lane + 128 * i), o),
+                    v[i], map_to_rank(bars.cl_full(cb), o));
+      }
+    }
+    if (in_bytes != 0u) {
+      // Finalise this rank's slots: the ranks' partials added in rank order
+      // (this rank's own from registers), then release the buffer to every
+      // peer.
+      if (!wt.wait_warp<false>(bars.cl_full(cb), cn & 1u)) return;
+#pragma unroll
+      for (int i = 0; i < SLOTS; ++i) {
+        if (!mine[i] || !has(i)) continue;
+        const float* src = cl + cb * (ks - 1) * nv + 4 * lane + 128 * i;
+        float4 acc = wk.rank == 0 ? v[i] : *reinterpret_cast<const float4*>(src);
+        for (int r = 1; r < ks; ++r)
+          add4(acc, r == wk.rank ? v[i]
+                                 : *reinterpret_cast<const float4*>(src + (r - (r > wk.rank ? 1 : 0)) * nv));
+        v[i] = acc;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        for (int r = 0; r < ks; ++r)
+          if (r != wk.rank) mbar_arrive_remote_relaxed(map_to_rank(bars.cl_empty(cb), r));
+      }
+    }
+    store = false;
+#pragma unroll
+    for (int i = 0; i < SLOTS; ++i) store = store || mine[i];
+    } else if (ks > 1) {
+      if (wk.rank != 0) {
+        if (!wt.wait_warp<false>(bars.cl_empty(cb), (cn & 1u) ^ 1u)) return;
+        const uint32_t dst0 =
+            map_to_rank(smem_addr(cl + (cb * (ks - 1) + (wk.rank - 1)) * nv + 4 * lane), 0);
+        const uint32_t bar0 = map_to_rank(bars.cl_full(cb), 0);
+#pragma unroll
+        for (int i = 0; i < SLOTS; ++i)
+          if (has(i)) st_async_v4(dst0 + 512 * i, v[i], bar0);
+        store = false;
+      } else {
+        if (!wt.wait_warp<false>(bars.cl_full(cb), cn & 1u)) return;
+        for (int p = 1; p < ks; ++p) {
+          const float* src = cl + (cb * (ks - 1) + (p - 1)) * nv + 4 * lane;
+#pragma unroll
+          for (int i = 0; i < SLOTS; ++i)
+            if (has(i)) add4(v[i], *reinterpret_cast<const float4*>(src + 128 * i));
+        }
+        __syncwarp();
+        if (lane == 0) {
+          for (int p = 1; p < ks; ++p) mbar_arrive_remote_relaxed(map_to_rank(bars.cl_empty(cb), p));
+        }
+      }
+    }
+    if (store && a.act != nullptr) {
+      // Lanes 4m + {0, 1} hold gate rows 0..7 of their tile and token, lanes
+      // 4m + {2, 3} the up rows of the same indices (rows 8..15).
+      const long long ni = a.N >> 1;
+#pragma unroll
+      for (int i = 0; i < SLOTS; ++i) {
+        float4 up;
+        up.x = __shfl_down_sync(0xffffffffu, v[i].x, 2);
+        up.y = __shfl_down_sync(0xffffffffu, v[i].y, 2);
+        up.z = __shfl_down_sync(0xffffffffu, v[i].z, 2);
+        up.w = __shfl_down_sync(0xffffffffu, v[i].w, 2);
+        if (mine[i] && has(i) && (vrow[i] & 8) == 0 && j * JT + vt[i] < wk.njobs) {
+          const long long idx = (wk.rt_begin + j * JT + vt[i]) * 8 + vrow[i];
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(silu_mul(v[i].x, up.x), silu_mul(v[i].y, up.y));
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(silu_mul(v[i].z, up.z), silu_mul(v[i].w, up.w));
+          uint2 pk;
+          pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+          pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(a.act + vtok[i] * ni + idx) = pk;
+        }
+      }
+      if (a.sync != nullptr) {
+        // One-launch layer: publish this hand-off's activations (every
+        // lane's stores, then one count) to the down phase's consumers.
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(a.sync, static_cast<unsigned>(min(JT, wk.njobs - j * JT)));
+      }
+    } else if (store) {
+#pragma unroll
+      for (int i = 0; i < SLOTS; ++i) {
+        if (mine[i] && has(i) && j * JT + vt[i] < wk.njobs) {
+          const long long row0 = (wk.rt_begin + j * JT + vt[i]) * 16;
+          const int tok = vtok[i], row = vrow[i];
+          const long long nrow = a.N - (row0 + row);  // rows left in y from this one
+          const float vv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+          if (a.y != nullptr) {
+            float* yp = a.y + static_cast<long long>(tok) * a.N + row0 + row;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              if (c < nrow) yp[c] = vv[c];
+          }
+          if (head) {
+            if (nrow >= 4) {
+              head_push4(hm[i], hs[i], ha[i], v[i], static_cast<int>(row0 + row));
+            } else {
+#pragma unroll
+              for (int c = 0; c < 3; ++c)
+                if (c < nrow) head_push(hm[i], hs[i], ha[i], vv[c], static_cast<int>(row0 + row + c));
+            }
+          }
+        }
+      }
+      if (topk) {
+        bool ok[SLOTS];
+        long long rbase[SLOTS];
+#pragma unroll
+        for (int i = 0; i < SLOTS; ++i) {
+          ok[i] = mine[i] && has(i) && j * JT + vt[i] < wk.njobs;
+          rbase[i] = (wk.rt_begin + j * JT + vt[i]) * 16 + vrow[i];
+        }
+        topk_update_thr<SLOTS>(a, tk_list, tk_buf, tk_cnt, lane, v, ok, rbase, vtok, tk_thr);
+      }
+    }
+    b += kEpiWarps;
+    if (b >= a.nbuf) { b -= a.nbuf; ++n; }
+  }
+  if (topk) {
+    for (int t = 0; t < T; ++t)
+      if (tk_cnt[t] > 0) (void)topk_flush_kth(tk_list, tk_buf, tk_cnt, t, lane, a.tk_k);
+  }
+  if (head && (RS || ks == 1 || wk.rank == 0)) head_finish_cta<SLOTS>(a, wk, ew, lane, hm, hs, ha, vtok);
 }
 
 // CONT: a phase of the one-launch layer; its hand-offs continue the CTA's
@@ -1663,11 +2093,26 @@ __global__ void __launch_bounds__(kThreads, 1) nq_gemv_kernel(const __grid_const
       mbar_init(bars.full(s), 1);
       mbar_init(bars.empty(s), kWarps);
     }
-    for (int b = 0; b < a.nbuf; ++b) {
-      mbar_init(bars.red_full(b), 32 * kWarps);
-      mbar_init(bars.red_empty(b), 32);
-      mbar_init(bars.cl_full(b), 1);   // rank 0's expect_tx; peers' bytes
-      mbar_init(bars.cl_empty(b), 1);  // rank 0, once per job
+    if constexpr (NTOK == kNtokXreg2) {
+      // The fused head with a K split finalises by reduce-scatter
+      // (epilogue_rs): each other finalising rank releases the buffer.
+      constexpr int kJt = kJobTiles<ROUTE, NTOK>;
+      const unsigned rel = (a.h_ws != nullptr && a.ksplit > 1)
+                               ? cl_empty_count<2 * kJt>(a.ksplit, kJt * 16 * a.T, wk.rank)
+                               : 1u;
+      for (int b = 0; b < a.nbuf; ++b) {
+        mbar_init(bars.red_full(b), 32 * kWarps);
+        mbar_init(bars.red_empty(b), 32);
+        mbar_init(bars.cl_full(b), 1);  // the finalising rank's expect_tx; peers' bytes
+        mbar_init(bars.cl_empty(b), rel);
+      }
+    } else {
+      for (int b = 0; b < a.nbuf; ++b) {
+        mbar_init(bars.red_full(b), 32 * kWarps);
+        mbar_init(bars.red_empty(b), 32);
+        mbar_init(bars.cl_full(b), 1);   // rank 0's expect_tx; peers' bytes
+        mbar_init(bars.cl_empty(b), 1);  // rank 0, once per job
+      }
     }
     *abort_flag = 0;
     for (int i = 0; i < 8; ++i) reinterpret_cast<uint32_t*>(smem + kZeroAreaOffset)[i] = 0u;
@@ -1698,7 +2143,14 @@ __global__ void __launch_bounds__(kThreads, 1) nq_gemv_kernel(const __grid_const
     constexpr int JT = kJobTiles<ROUTE, NTOK>;
     constexpr int kTokBlocks =
         (ROUTE == kRouteMma && (NTOK == 2 || NTOK == kNtokXreg2 || NTOK == kNtokXregH)) ? 2 : 1;
-    epilogue<JT * kTokBlocks, JT>(a, smem, bars, wt, wk, ew, lane);
+    if constexpr (NTOK == kNtokXreg2) {
+      if (a.h_ws != nullptr && a.ksplit > 1)
+        epilogue_rs<JT * kTokBlocks, JT>(a, smem, bars, wt, wk, ew, lane);
+      else
+        epilogue<JT * kTokBlocks, JT>(a, smem, bars, wt, wk, ew, lane);
+    } else {
+      epilogue<JT * kTokBlocks, JT>(a, smem, bars, wt, wk, ew, lane);
+    }
   } else {
     griddep_wait();
     if constexpr (ROUTE == kRouteMma && NTOK == kNtokXreg) {

@@ -927,8 +927,8 @@ int nq_head_workspace_bytes(size_t* bytes) {
   if (!bytes) return NQ_EINVAL;
   DevInfo* d;
   if (int rc = dev_info(&d)) return rc;
-  // one state per (cluster, epilogue warp, token) and per (group of
-  // kHeadGroup clusters, token); clusters <= SMs
+  // one state per (CTA, epilogue warp, token) and per (group of
+  // kHeadGroup CTAs, token); CTAs <= SMs
   const size_t groups = (static_cast<size_t>(d->sms) + kHeadGroup - 1) / kHeadGroup;
   *bytes = static_cast<size_t>(kHeadCounterBytes) +
            (static_cast<size_t>(d->sms) * kEpiWarps + groups) * kHeadMaxT * kHeadStateBytes;
@@ -949,7 +949,7 @@ static int head_launch(const void* packed, const uint16_t* scales, const void* x
   {
     DevInfo* d;
     if (int rc = dev_info(&d)) return rc;
-    if (d->sms > kHeadGroup * kHeadMaxGroups) return NQ_EUNSUPPORTED;  // merge covers 256 clusters
+    if (d->sms > kHeadGroup * kHeadMaxGroups) return NQ_EUNSUPPORTED;  // merge covers 256 CTAs
   }
   if (!aligned16(packed) || !aligned16(scales) || !aligned16(x_bf16) || !aligned16(workspace) ||
       (y && !aligned16(y)))
@@ -985,7 +985,10 @@ static int head_launch(const void* packed, const uint16_t* scales, const void* x
     h.tk_bufs = h.tk_lists + static_cast<size_t>(d->sms) * kEpiWarps * kHeadMaxT * 32;
   }
   if (int rc = launch_plan(p, packed, scales, x_bf16, y, K, N, T, st, h)) return rc;
-  if (k > 0 && launch_topk_merge(h.tk_lists, p.clusters * kEpiWarps, T, k, topk_idx, topk_val,
+  // one list per (unit, epilogue warp): per CTA where the kernel finalises by
+  // reduce-scatter (two token blocks in registers, K split), else per cluster
+  const int units = p.clusters * (p.ntok == kNtokXreg2 && p.ks > 1 ? p.ks : 1);
+  if (k > 0 && launch_topk_merge(h.tk_lists, units * kEpiWarps, T, k, topk_idx, topk_val,
                                  env_int("NQ_PDL", 1) != 0, st) != cudaSuccess) {
     (void)cudaGetLastError();
     return NQ_ECUDA;
@@ -1006,8 +1009,8 @@ int nq_head_topk_workspace_bytes(size_t* bytes) {
   if (int rc = nq_head_workspace_bytes(&head_bytes)) return rc;
   DevInfo* d;
   if (int rc = dev_info(&d)) return rc;
-  // then per (cluster, epilogue warp, token) a list of 32 keys, then a
-  // candidate buffer of 64 keys; clusters <= SMs
+  // then per (CTA, epilogue warp, token) a list of 32 keys, then a
+  // candidate buffer of 64 keys; CTAs <= SMs
   *bytes = static_cast<size_t>(align_up(static_cast<int>(head_bytes), 256)) +
            static_cast<size_t>(d->sms) * kEpiWarps * kHeadMaxT * (32 + 64) * sizeof(unsigned long long);
   return NQ_OK;

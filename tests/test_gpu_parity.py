@@ -134,7 +134,7 @@ def test_gemv_ffma_parity(bits, T):
 
 
 @pytest.mark.parametrize("ksplit", [1, 2, 4, 8])
-@pytest.mark.parametrize("T", [1, 8, 16])
+@pytest.mark.parametrize("T", [1, 5, 8, 12, 16])
 def test_gemv_ksplit_parity(ksplit, T):
     case = uniform_case((305, ksplit, T), 5, 300, 17408 // 8, T)
     packed, sp = device_weight(nqp, torch, case, DEV)

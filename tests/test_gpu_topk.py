@@ -60,7 +60,7 @@ SHAPES = [(6, 1024, 1000), (6, 512, 17), (4, 2048, 300), (5, 1024, 1), (8, 1024,
           (5, 17408, 100)]   # the last one runs as clusters of 4 CTAs (K split)
 
 
-@pytest.mark.parametrize("T", [1, 2, 8, 9, 16])
+@pytest.mark.parametrize("T", [1, 2, 5, 8, 9, 12, 16])
 def test_topk_matches_own_logits_and_oracle(T):
     for i, (bits, K, N) in enumerate(SHAPES):
         case = rtn_case((520, T, i), bits, N, K, T)
