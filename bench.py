@@ -626,26 +626,75 @@ def run_ours(args, rank, world, local_rank):
     encoders = encoder_times(torch, nqp, dev) if rank == 0 else None
 
     # ---------------- end to end: x from pinned host, logits back to pinned host
+    # Every step uploads its x arena and reads back its logits inside the timed
+    # region.  Two buffer sets (x arena and outputs, each with its own graphs)
+    # let step s + 1's upload and step s's read-back run on copy streams while
+    # the GEMVs of the neighbouring step run, as a decode loop would pipeline
+    # them; a set is reused only after its previous step's GEMVs and
+    # read-backs have finished.
     x_host = torch.empty(x_arena.shape, dtype=x_arena.dtype, pin_memory=True)
     x_host.copy_(x_arena)
     y_host = {T: torch.empty((T, VOCAB), dtype=torch.float32, pin_memory=True) for T in TS}
     h2d = x_arena.numel() * x_arena.element_size()
     d2h = sum(T * VOCAB * 4 for T in TS)
-    e2e_steps = max(3, min(args.steps, 50))
+    x_arena2 = x_arena.clone()
+    entries2, off = [], 0
+    for e in entries:
+        entries2.append(dict(e, x=x_arena2[off:off + 16 * e["K"]].view(16, e["K"])))
+        off += 16 * e["K"]
+    ys2 = {k: torch.empty_like(v) for k, v in ys.items()}
+    graphs2 = {(T, k): capture(torch, nqp, entries2, ys2, T, k, stream)[0] for T in TS for k in KINDS}
+    sets = [(x_arena, ys, graphs), (x_arena2, ys2, graphs2)]
+    up = torch.cuda.Stream(device=dev)     # host -> device
+    down = torch.cuda.Stream(device=dev)   # device -> host
+
+    def e2e_steps_run(nsteps, e_start=None, e_end=None):
+        comp_done = [None, None]   # the set's last step: GEMVs finished (x no longer read)
+        read_done = [None, None]   # the set's last step: logits read back (outputs free)
+        first = torch.cuda.Event()
+        first.record(stream)
+        if e_start is not None:
+            e_start.record(stream)
+        up.wait_event(first)
+        down.wait_event(first)
+        for s_ in range(nsteps):
+            xa, yb, gb = sets[s_ % 2]
+            with torch.cuda.stream(up):
+                if comp_done[s_ % 2] is not None:
+                    up.wait_event(comp_done[s_ % 2])
+                xa.copy_(x_host, non_blocking=True)
+                x_ready = torch.cuda.Event()
+                x_ready.record(up)
+            with torch.cuda.stream(stream):
+                stream.wait_event(x_ready)
+                if read_done[s_ % 2] is not None:
+                    stream.wait_event(read_done[s_ % 2])
+                for T in TS:
+                    for k in KINDS:
+                        gb[(T, k)].replay()
+                    head_done = torch.cuda.Event()
+                    head_done.record(stream)
+                    with torch.cuda.stream(down):
+                        down.wait_event(head_done)
+                        y_host[T].copy_(yb["head"][:T], non_blocking=True)
+                comp_done[s_ % 2] = torch.cuda.Event()
+                comp_done[s_ % 2].record(stream)
+            read_done[s_ % 2] = torch.cuda.Event()
+            read_done[s_ % 2].record(down)
+        stream.wait_event(read_done[(nsteps - 1) % 2])
+        if e_end is not None:
+            e_end.record(stream)
+        stream.synchronize()
+
+    e2e_run_steps = max(3, min(args.steps, 50))
+    e2e_run_steps += e2e_run_steps % 2           # both sets equally often
+    e2e_steps_run(4)                             # warm-up: both sets' graphs uploaded
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            x_arena.copy_(x_host, non_blocking=True)
-            for T in TS:
-                for k in KINDS:
-                    graphs[(T, k)].replay()
-                y_host[T].copy_(ys["head"][:T], non_blocking=True)
-        e1.record(stream)
-    stream.synchronize()
+    e2e_steps_run(e2e_run_steps, e0, e1)
+    e2e_steps = e2e_run_steps
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
 
     if rank != 0:
