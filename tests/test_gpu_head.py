@@ -160,8 +160,31 @@ def test_head_workspace_errors():
     assert nqp.last_device_error() == 0
 
 
+def test_head_reduce_scatter_k_split():
+    """6-bit codes, K = 5120, T = 16: both token blocks in registers at K
+    split 2, the kernel whose epilogue finalises by reduce-scatter (each rank
+    of a cluster takes a slot of every hand-off and publishes its own
+    states).  Fused results against the kernel's own logits, logits against
+    the oracle, and argmax / maximum against the plain GEMV's logits."""
+    K, N, bits, T = 5120, 16 * 187 + 7, 6, 16   # (at T = 15 the hybrid still fits)
+    p = nqp.plan(K, N, T, bits)
+    assert (p["x"], p["ksplit"]) == ("regs2", 2), p
+    case = rtn_case((506, T), bits, N, K, T)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    y, am, mx, lse = _head(case, packed, sp)
+    head_check_self(y, am, mx, lse)
+    _check_oracle(case, am, mx, lse)
+    x = device_x(torch, case, DEV)[:T].contiguous()
+    y2 = torch.full((T, N), float("nan"), dtype=torch.float32, device=DEV)
+    nqp.gemv(packed, sp, x, y2, K, N, T, bits)
+    assert np.array_equal(y2.cpu().numpy().view(np.uint32), y.view(np.uint32))
+    _, am2, mx2, lse2 = _head(case, packed, sp, store_y=False)
+    assert np.array_equal(am, am2) and np.array_equal(mx.view(np.uint32), mx2.view(np.uint32))
+    assert np.array_equal(lse.view(np.uint32), lse2.view(np.uint32))
+
+
 @pytest.mark.slow
-@pytest.mark.parametrize("T", [1, 8])
+@pytest.mark.parametrize("T", [1, 8, 16])
 def test_head_full_size(T):
     """The 248,320-row 6-bit output head: fused results against the kernel's own
     logits (all rows), and the logits of sampled rows against the oracle."""

@@ -75,6 +75,22 @@ def test_topk_matches_own_logits_and_oracle(T):
             _check_oracle(case, k, idx, val)
 
 
+def test_topk_reduce_scatter_k_split():
+    """The top-k of the kernel that finalises by reduce-scatter (6-bit, K =
+    5120, T = 16, both token blocks in registers at K split 2): one list per CTA and
+    epilogue warp, merged; against the kernel's own logits and the oracle."""
+    K, N, bits, T = 5120, 16 * 187 + 7, 6, 16
+    assert (nqp.plan(K, N, T, bits)["x"], nqp.plan(K, N, T, bits)["ksplit"]) == ("regs2", 2)
+    case = rtn_case((521, T), bits, N, K, T)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    for k in (1, 8, 32):
+        y, (idx, val, am, mx, lse) = _topk(case, packed, sp, k)
+        _check_self(y, k, idx, val)
+        head_check_self(y, am, mx, lse)
+        assert np.array_equal(idx[:, 0], am)
+        _check_oracle(case, k, idx, val)
+
+
 def test_topk_without_logits_and_repeat_calls():
     case = uniform_case((521,), 5, 3000, 2048, 8)
     packed, sp = device_weight(nqp, torch, case, DEV)
