@@ -183,6 +183,46 @@ def test_head_reduce_scatter_k_split():
     assert np.array_equal(lse.view(np.uint32), lse2.view(np.uint32))
 
 
+def test_head_reduce_scatter_in_graph():
+    """The reduce-scatter head and its top-k captured into one CUDA graph and
+    replayed twice (the exchange barriers' phases and the arrival counters
+    carry over between replays): bitwise the eager calls' results."""
+    K, N, bits, T = 5120, 16 * 131 + 3, 6, 16
+    case = rtn_case((507,), bits, N, K, T)
+    packed, sp = device_weight(nqp, torch, case, DEV)
+    x = device_x(torch, case, DEV)[:T].contiguous()
+    ws = torch.empty(nqp.head_topk_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    outs = [torch.empty(T, dtype=dt, device=DEV) for dt in (torch.int32, torch.float32, torch.float32)]
+    tki = torch.empty((T, 8), dtype=torch.int32, device=DEV)
+    tkv = torch.empty((T, 8), dtype=torch.float32, device=DEV)
+    stream = torch.cuda.Stream(device=DEV)
+
+    def run():
+        nqp.gemv_head_topk(packed, sp, x, K, N, T, bits, 8, workspace=ws, topk_idx=tki,
+                           topk_val=tkv, argmax=outs[0], maxval=outs[1], lse=outs[2],
+                           stream=stream)
+    with torch.cuda.stream(stream):
+        run()
+    stream.synchronize()
+    ref = [o.clone() for o in outs] + [tki.clone(), tkv.clone()]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run()
+    for _ in range(2):
+        for o in outs + [tki, tkv]:
+            o.fill_(0)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+        assert nqp.last_device_error() == 0
+        for a, b in zip(ref, outs + [tki, tkv]):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    _, am, mx, lse = _head(case, packed, sp)
+    assert np.array_equal(am, ref[0].cpu().numpy())
+    assert np.array_equal(tki.cpu().numpy()[:, 0], am)
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("T", [1, 8, 16])
 def test_head_full_size(T):
