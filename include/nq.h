@@ -50,9 +50,11 @@
  *   - Environment switches, read at each call (for experiments; the defaults
  *     are the measured best): NQ_ROUTE (auto | mma | ffma), NQ_KSPLIT (0 =
  *     the planner's K split, else 1, 2, 4 or 8), NQ_X_F16 (1: fp16 route of
- *     4-bit codes at T <= 2; 0: bf16 route), NQ_PDL (1: programmatic
- *     dependent launch), NQ_WAIT_MS (bound of every in-kernel wait, default
- *     2000).
+ *     4-bit codes at T <= 2; 0: bf16 route), NQ_XREGH (T > 8: unset = the
+ *     planner's choice between both token blocks in registers and the hybrid,
+ *     0 = never the hybrid, 1 = only the hybrid), NQ_MLP_FUSED (1: nq_mlp in
+ *     one launch where it can), NQ_PDL (1: programmatic dependent launch),
+ *     NQ_WAIT_MS (bound of every in-kernel wait, default 2000).
  *
  * PACKED LAYOUT (version 2)
  * -------------------------
