@@ -1667,38 +1667,34 @@ __device__ __forceinline__ unsigned cl_empty_count(int ks, int nv, int rank) {
   return max(1, __popc(slot_owners<SLOTS>(ks, nv) & ~(1u << rank)));
 }
 
-// CONT: a phase of the one-launch layer; its hand-offs continue the CTA's
-// sequence after `h0` hand-offs of the previous phase (hand-off g uses
-// buffer g % nbuf and belongs to epilogue warp g % kEpiWarps).
 // The epilogue of the fused head whose K split finalises by reduce-scatter
-// (two token blocks in registers; see slot_owners).  Besides the exchange it
-// differs from epilogue() in the softmax update (head_push4) and in keeping
-// the top-k thresholds in registers; a separate function, so that the
-// other kernels' code stays as it is.
+// (two token blocks in registers, ksplit > 1; see slot_owners).  Besides the
+// exchange it differs from epilogue() in the softmax update (head_push4), in
+// keeping the top-k thresholds in registers and in publishing head states and
+// top-k lists per CTA; a separate function, so that the other kernels' code
+// stays as it is.
 template <int SLOTS, int JT>
 __device__ inline void epilogue_rs(const GemvArgs& a, uint8_t* smem, const Bars& bars,
                                    const Waiter& wt, const Work& wk, int ew, int lane) {
-  constexpr bool CONT = false, RS = true;
-  const int h0 = 0;
   const int T = a.T;
   const int nvt = 16 * T;            // values per row tile (a multiple of 16)
   const int nv = JT * nvt;           // values per hand-off (JT consecutive tiles)
   const int ks = a.ksplit;
   const float* red = reinterpret_cast<const float*>(smem + a.off_red);
   float* cl = reinterpret_cast<float*>(smem + a.off_cl);
-  const uint32_t cl_bytes = static_cast<uint32_t>((ks - 1) * nv * 4);
-  // Reduce-scatter (RS, ks > 1): mine[i] = this rank finalises slot i;
-  // in_bytes = what its peers send it per hand-off.
+  // mine[i]: this rank finalises slot i; in_bytes: what its peers send it per
+  // hand-off; sends: some other rank finalises a slot in use.
   bool mine[SLOTS];
   uint32_t in_bytes = 0;
+  bool any_mine = false;
 #pragma unroll
   for (int i = 0; i < SLOTS; ++i) {
-    mine[i] = !RS || ks == 1 || i % ks == wk.rank;
-    if (RS && ks > 1 && mine[i]) in_bytes += static_cast<uint32_t>((ks - 1) * slot_values(nv, i) * 4);
+    mine[i] = i % ks == wk.rank;
+    any_mine = any_mine || mine[i];
+    if (mine[i]) in_bytes += static_cast<uint32_t>((ks - 1) * slot_values(nv, i) * 4);
   }
-  const bool sends = RS && ks > 1 && (slot_owners<SLOTS>(ks, nv) & ~(1u << wk.rank)) != 0u;
+  const bool sends = (slot_owners<SLOTS>(ks, nv) & ~(1u << wk.rank)) != 0u;
   auto has = [&](int i) { return 4 * lane + 128 * i < nv; };
-  const bool head = a.h_ws != nullptr;
   float hm[SLOTS], hs[SLOTS];
   int ha[SLOTS];
 #pragma unroll
@@ -1718,7 +1714,7 @@ __device__ inline void epilogue_rs(const GemvArgs& a, uint8_t* smem, const Bars&
     vrow[i] = rest & 15;
   }
   const int njt = (wk.njobs + JT - 1) / JT;  // hand-offs of this CTA
-  const bool topk = head && a.tk_k > 0 && (RS || ks == 1 || wk.rank == 0);
+  const bool topk = a.tk_k > 0;
   unsigned long long* tk_list = nullptr;
   unsigned long long* tk_buf = nullptr;
   int* tk_cnt = nullptr;
@@ -1726,8 +1722,7 @@ __device__ inline void epilogue_rs(const GemvArgs& a, uint8_t* smem, const Bars&
 #pragma unroll
   for (int i = 0; i < SLOTS; ++i) tk_thr[i] = 0ull;
   if (topk) {
-    // one list per CTA (RS: the ranks finalise different rows), else per cluster
-    const size_t me = static_cast<size_t>(RS ? blockIdx.x : blockIdx.x / ks) * kEpiWarps + ew;
+    const size_t me = static_cast<size_t>(blockIdx.x) * kEpiWarps + ew;  // one list per CTA
     tk_list = a.tk_lists + me * kHeadMaxT * 32;
     tk_buf = a.tk_bufs + me * kHeadMaxT * 64;
     tk_cnt = reinterpret_cast<int*>(smem + a.off_tk) + ew * kHeadMaxT;
@@ -1735,26 +1730,10 @@ __device__ inline void epilogue_rs(const GemvArgs& a, uint8_t* smem, const Bars&
     if (lane < T) tk_cnt[lane] = 0;
     __syncwarp();
   }
-  int b = ew;        // buffer of hand-off j (j % nbuf)
+  int b = ew;        // buffer of hand-off j (j % nbuf), also its exchange buffer
   uint32_t n = 0;    // uses of that buffer so far (j / nbuf)
-  int j = ew;
-  if constexpr (CONT) {
-    j = (ew - h0 % kEpiWarps + kEpiWarps) % kEpiWarps;  // first local hand-off of this warp
-    b = (h0 + j) % a.nbuf;
-    n = static_cast<uint32_t>((h0 + j) / a.nbuf);
-  }
-  for (; j < njt; j += kEpiWarps) {
-    // Cluster-exchange buffer of this hand-off: its position among this
-    // launch's K-split hand-offs, the same on every rank (a continuing phase
-    // starts its own count; its red buffers continue the CTA's count).
-    const int cb = CONT ? j % a.nbuf : b;
-    const uint32_t cn = CONT ? static_cast<uint32_t>(j / a.nbuf) : n;
-    if constexpr (RS) {
-      if (in_bytes != 0u && lane == 0) mbar_arrive_expect_tx_relaxed(bars.cl_full(cb), in_bytes);
-    } else {
-      if (ks > 1 && wk.rank == 0 && lane == 0)
-        mbar_arrive_expect_tx_relaxed(bars.cl_full(cb), cl_bytes);
-    }
+  for (int j = ew; j < njt; j += kEpiWarps) {
+    if (in_bytes != 0u && lane == 0) mbar_arrive_expect_tx_relaxed(bars.cl_full(b), in_bytes);
     if (!wt.wait_warp<false>(bars.red_full(b), n & 1u)) return;
     float4 v[SLOTS];
 #pragma unroll
@@ -1766,33 +1745,29 @@ __device__ inline void epilogue_rs(const GemvArgs& a, uint8_t* smem, const Bars&
         for (int w = 0; w < kWarps; ++w) add4(v[i], *reinterpret_cast<const float4*>(p + w * nv));
       }
     }
-    // Every lane has consumed its loads of the slot (the sums above); a
-    // release here would also wait for the previous job's y stores.
     mbar_arrive_relaxed(bars.red_empty(b));  // every lane: count 32
-    bool store = true;
-    if constexpr (RS) {
     if (sends) {
       // Partials of the slots other ranks finalise: peer r of slot i's owner
       // o writes area r - (r > o) of o's exchange buffer.
-      if (!wt.wait_warp<false>(bars.cl_empty(cb), (cn & 1u) ^ 1u)) return;
+      if (!wt.wait_warp<false>(bars.cl_empty(b), (n & 1u) ^ 1u)) return;
 #pragma unroll
       for (int i = 0; i < SLOTS; ++i) {
         if (mine[i] || !has(i)) continue;
         const int o = i % ks;
         const int area = wk.rank - (wk.rank > o ? 1 : 0);
-        st_async_v4(map_to_rank(smem_addr(cl + (cb * (ks - 1) + area) * nv + 4 * lane + 128 * i), o),
-                    v[i], map_to_rank(bars.cl_full(cb), o));
+        st_async_v4(map_to_rank(smem_addr(cl + (b * (ks - 1) + area) * nv + 4 * lane + 128 * i), o),
+                    v[i], map_to_rank(bars.cl_full(b), o));
       }
     }
     if (in_bytes != 0u) {
       // Finalise this rank's slots: the ranks' partials added in rank order
       // (this rank's own from registers), then release the buffer to every
       // peer.
-      if (!wt.wait_warp<false>(bars.cl_full(cb), cn & 1u)) return;
+      if (!wt.wait_warp<false>(bars.cl_full(b), n & 1u)) return;
 #pragma unroll
       for (int i = 0; i < SLOTS; ++i) {
         if (!mine[i] || !has(i)) continue;
-        const float* src = cl + cb * (ks - 1) * nv + 4 * lane + 128 * i;
+        const float* src = cl + b * (ks - 1) * nv + 4 * lane + 128 * i;
         float4 acc = wk.rank == 0 ? v[i] : *reinterpret_cast<const float4*>(src);
         for (int r = 1; r < ks; ++r)
           add4(acc, r == wk.rank ? v[i]
@@ -1802,65 +1777,10 @@ __device__ inline void epilogue_rs(const GemvArgs& a, uint8_t* smem, const Bars&
       __syncwarp();
       if (lane == 0) {
         for (int r = 0; r < ks; ++r)
-          if (r != wk.rank) mbar_arrive_remote_relaxed(map_to_rank(bars.cl_empty(cb), r));
+          if (r != wk.rank) mbar_arrive_remote_relaxed(map_to_rank(bars.cl_empty(b), r));
       }
     }
-    store = false;
-#pragma unroll
-    for (int i = 0; i < SLOTS; ++i) store = store || mine[i];
-    } else if (ks > 1) {
-      if (wk.rank != 0) {
-        if (!wt.wait_warp<false>(bars.cl_empty(cb), (cn & 1u) ^ 1u)) return;
-        const uint32_t dst0 =
-            map_to_rank(smem_addr(cl + (cb * (ks - 1) + (wk.rank - 1)) * nv + 4 * lane), 0);
-        const uint32_t bar0 = map_to_rank(bars.cl_full(cb), 0);
-#pragma unroll
-        for (int i = 0; i < SLOTS; ++i)
-          if (has(i)) st_async_v4(dst0 + 512 * i, v[i], bar0);
-        store = false;
-      } else {
-        if (!wt.wait_warp<false>(bars.cl_full(cb), cn & 1u)) return;
-        for (int p = 1; p < ks; ++p) {
-          const float* src = cl + (cb * (ks - 1) + (p - 1)) * nv + 4 * lane;
-#pragma unroll
-          for (int i = 0; i < SLOTS; ++i)
-            if (has(i)) add4(v[i], *reinterpret_cast<const float4*>(src + 128 * i));
-        }
-        __syncwarp();
-        if (lane == 0) {
-          for (int p = 1; p < ks; ++p) mbar_arrive_remote_relaxed(map_to_rank(bars.cl_empty(cb), p));
-        }
-      }
-    }
-    if (store && a.act != nullptr) {
-      // Lanes 4m + {0, 1} hold gate rows 0..7 of their tile and token, lanes
-      // 4m + {2, 3} the up rows of the same indices (rows 8..15).
-      const long long ni = a.N >> 1;
-#pragma unroll
-      for (int i = 0; i < SLOTS; ++i) {
-        float4 up;
-        up.x = __shfl_down_sync(0xffffffffu, v[i].x, 2);
-        up.y = __shfl_down_sync(0xffffffffu, v[i].y, 2);
-        up.z = __shfl_down_sync(0xffffffffu, v[i].z, 2);
-        up.w = __shfl_down_sync(0xffffffffu, v[i].w, 2);
-        if (mine[i] && has(i) && (vrow[i] & 8) == 0 && j * JT + vt[i] < wk.njobs) {
-          const long long idx = (wk.rt_begin + j * JT + vt[i]) * 8 + vrow[i];
-          const __nv_bfloat162 lo = __floats2bfloat162_rn(silu_mul(v[i].x, up.x), silu_mul(v[i].y, up.y));
-          const __nv_bfloat162 hi = __floats2bfloat162_rn(silu_mul(v[i].z, up.z), silu_mul(v[i].w, up.w));
-          uint2 pk;
-          pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-          pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-          *reinterpret_cast<uint2*>(a.act + vtok[i] * ni + idx) = pk;
-        }
-      }
-      if (a.sync != nullptr) {
-        // One-launch layer: publish this hand-off's activations (every
-        // lane's stores, then one count) to the down phase's consumers.
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) atomicAdd(a.sync, static_cast<unsigned>(min(JT, wk.njobs - j * JT)));
-      }
-    } else if (store) {
+    if (any_mine) {
 #pragma unroll
       for (int i = 0; i < SLOTS; ++i) {
         if (mine[i] && has(i) && j * JT + vt[i] < wk.njobs) {
@@ -1874,14 +1794,12 @@ __device__ inline void epilogue_rs(const GemvArgs& a, uint8_t* smem, const Bars&
             for (int c = 0; c < 4; ++c)
               if (c < nrow) yp[c] = vv[c];
           }
-          if (head) {
-            if (nrow >= 4) {
-              head_push4(hm[i], hs[i], ha[i], v[i], static_cast<int>(row0 + row));
-            } else {
+          if (nrow >= 4) {
+            head_push4(hm[i], hs[i], ha[i], v[i], static_cast<int>(row0 + row));
+          } else {
 #pragma unroll
-              for (int c = 0; c < 3; ++c)
-                if (c < nrow) head_push(hm[i], hs[i], ha[i], vv[c], static_cast<int>(row0 + row + c));
-            }
+            for (int c = 0; c < 3; ++c)
+              if (c < nrow) head_push(hm[i], hs[i], ha[i], vv[c], static_cast<int>(row0 + row + c));
           }
         }
       }
@@ -1903,7 +1821,7 @@ __device__ inline void epilogue_rs(const GemvArgs& a, uint8_t* smem, const Bars&
     for (int t = 0; t < T; ++t)
       if (tk_cnt[t] > 0) (void)topk_flush_kth(tk_list, tk_buf, tk_cnt, t, lane, a.tk_k);
   }
-  if (head && (RS || ks == 1 || wk.rank == 0)) head_finish_cta<SLOTS>(a, wk, ew, lane, hm, hs, ha, vtok);
+  head_finish_cta<SLOTS>(a, wk, ew, lane, hm, hs, ha, vtok);
 }
 
 // CONT: a phase of the one-launch layer; its hand-offs continue the CTA's
