@@ -58,7 +58,7 @@ SHAPES = [(6, 1024, 1000), (6, 512, 17), (4, 2048, 300), (5, 1024, 1), (6, 17408
 
 # T = 5 and 12: the second value slot of a hand-off is partly filled (the K
 # split's reduce-scatter sends it to rank 1 for some lanes only)
-@pytest.mark.parametrize("T", [1, 2, 3, 5, 8, 9, 12, 16])
+@pytest.mark.parametrize("T", [1, 2, 3, 5, 8, 9, 12, 15, 16])
 def test_head_matches_gemv_and_oracle(T):
     for i, (bits, K, N) in enumerate(SHAPES):
         case = rtn_case((500, T, i), bits, N, K, T)

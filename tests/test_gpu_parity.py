@@ -162,7 +162,7 @@ HYBRID_SHAPES = [(2560, 300, 1), (1088, 37, 1), (4096, 170, 2), (8192, 50, 4)]
 
 
 @pytest.mark.parametrize("bits", [4, 5, 6, 8])
-@pytest.mark.parametrize("T", [9, 11, 16])
+@pytest.mark.parametrize("T", [9, 11, 13, 15, 16])
 def test_hybrid_x_parity(bits, T, monkeypatch):
     """T > 8 through the kernel that keeps tokens 0-7 in registers and tokens
     8.. in shared memory: ragged row tiles, uneven warp slices, K splits 1 to
